@@ -1,0 +1,204 @@
+/*
+ * locks.h -- C ABI of the LOCKS sparse long-context decode library (GB300, sm_103a).
+ *
+ * Method: "LOCKS: Page-Local Compact Key Summaries for Efficient Long-Context
+ * Decoding" (J. Hwang, arXiv 2607.24555).  Section references below are to
+ * that paper's technical summary:
+ *   §2 "Method: LOCKS" -- page-local spectral decomposition, quantisation,
+ *      reconstruction and selection (the equation for s_j(q)), group-shared
+ *      selection (GQA), implementation notes (full CUDA graph, summaries built
+ *      off the decode critical path when a page is finalised);
+ *   abstract -- "estimates each page's attention mass by log-sum-exp, and
+ *      attends only the top pages; selection itself reads no candidate keys
+ *      or values" (paraphrased).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or synchronises inside the decode entry points, so
+ *    a sequence of calls can be captured into a CUDA graph.  Every call is
+ *    asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - All device pointers must be 16-byte aligned.
+ *  - Host-side validation runs before any launch; on failure nothing is
+ *    launched and an error code is returned.  A failed launch returns
+ *    LOCKS_ERR_CUDA.
+ *  - Data-dependent problems found on the device (a block id outside
+ *    [0, num_blocks), a sequence longer than its block-table row, a wait that
+ *    ran out) never fault: the kernel skips the offending access and ORs a
+ *    LOCKS_FLAG_* bit into the status word at the start of `workspace`;
+ *    locks_read_status() returns it (that call synchronises `stream`).
+ *  - Fixed shape: head_dim d = 128, page_size B = 16, rank r = 8, quantised
+ *    summaries; group_size G = 4.  Other values return LOCKS_ERR_UNSUPPORTED.
+ *
+ * Tensor layouts
+ * --------------
+ *  q            bf16 [batch][H_kv*G][128]; query head h*G+g belongs to KV head h.
+ *  k_cache,
+ *  v_cache      bf16 [num_blocks][H_kv][16][128]; one physical block holds one
+ *               16-token page for every KV head; a page-head is 4096 contiguous
+ *               bytes.
+ *  block_table  int32 [batch][max_pages]; logical page j of request b lives in
+ *               physical block block_table[b][j].
+ *  seq_lens     int32 [batch]; L_b = tokens cached for request b INCLUDING the
+ *               token being decoded (its K/V already written).  Full pages:
+ *               n_b = L_b / 16; the tail page n_b holds t_b = L_b % 16 tokens
+ *               (none when t_b = 0) and has no summary yet.
+ *  summaries    uint8 [num_blocks][H_kv][784]; record of page-head (blk, h) at
+ *               byte (blk*H_kv + h)*784.  Only blocks passed to
+ *               locks_build_summaries hold valid records.
+ *  scores       fp32 [batch][H_kv][max_pages][G]; s_j for full pages j < n_b.
+ *  selected     int32 [batch][H_kv][budget_pages]; logical page indices, sorted
+ *               ascending; only the first n_selected[b][h] entries are valid.
+ *  n_selected   int32 [batch][H_kv] = min(budget_pages, n_b).
+ *  out          fp32 [batch][H_kv*G][128].
+ *
+ * Summary record (784 bytes per page-head; ~9.6 % of the page-head's 8192 KV
+ * bytes, §2 "about 10 % at B = 16, r = 8")
+ * ---------------------------------------------------------------------------
+ *  The page's 16 keys k_i are centred on mu = mean_i k_i; X = K - mu.  The
+ *  top-8 eigenpairs (lambda_k, w_k) of the 16x16 Gram matrix X X^T give the
+ *  orthonormal key-space basis V[:,k] = X^T w_k / sqrt(lambda_k) and the token
+ *  coefficients c[i,k] = w_k[i] sqrt(lambda_k); directions with
+ *  lambda_k <= 1e-6 lambda_1 are zero.  Sign: for each k the coefficient of
+ *  largest magnitude over the 16 tokens is positive.  Quantisation is
+ *  symmetric with one fp32 scale per tensor: s = max|x| / qmax, code =
+ *  round-half-even(x / s) (s = 0 gives codes 0); V: int4 in [-7, 7]
+ *  (two's-complement nibbles), mu and c: int8 in [-127, 127].
+ *  Byte map (d = 0..127, k = 0..7, i = 0..15):
+ *   [0,512)   V code (dim, k): s = dim/16, w = dim%16, hh = w/8, t = (w%8)/2,
+ *             e = w%2, p = s/2, sp = s%2, m = 2*sp + hh + 4*e;
+ *             byte 64*k + 16*t + 4*p + m/2, high nibble iff m is odd.
+ *   [512,640) mu code (dim): byte 512 + 32*t + 4*s + 2*hh + e.
+ *   [640,768) c code (i, k): nt = i/8, gid = i%8, tk = k/2, ek = k%2;
+ *             byte 640 + 4*(4*gid + tk) + 2*nt + ek.
+ *   [768,784) fp32 little-endian: s_V, s_mu, s_c, tail energy
+ *             sum_{k>8} lambda_k (diagnostic of §3 Thm. 1; not used by scoring).
+ *  The byte map puts each lane's share of a tensor-core fragment in one
+ *  contiguous 16/32/4-byte run, so the scorer loads it with single vector loads.
+ */
+#ifndef LOCKS_H
+#define LOCKS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *locks_stream_t;
+
+typedef enum {
+  LOCKS_OK = 0,
+  LOCKS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, ... */
+  LOCKS_ERR_UNSUPPORTED = 2,  /* a shape this build does not implement */
+  LOCKS_ERR_WORKSPACE = 3,    /* workspace smaller than locks_workspace_bytes */
+  LOCKS_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  LOCKS_ERR_TIMEOUT = 5       /* reserved: returned by locks_read_status callers */
+} locks_status;
+
+typedef struct {
+  int32_t head_dim;      /* d: 128 */
+  int32_t page_size;     /* B: 16 */
+  int32_t rank;          /* r: 8 */
+  int32_t num_kv_heads;  /* H_kv >= 1 */
+  int32_t group_size;    /* G: 4 query heads per KV head */
+  int32_t quant;         /* 1: int4 basis, int8 centroid/coefficients */
+} locks_cfg;
+
+/* Status-word bits written by the kernels (see locks_read_status). */
+#define LOCKS_FLAG_BAD_BLOCK   1u  /* a block id outside [0, num_blocks) was skipped */
+#define LOCKS_FLAG_BAD_SEQLEN  2u  /* L_b < 0 or ceil(L_b/16) > max_pages; request skipped */
+#define LOCKS_FLAG_TIMEOUT     4u  /* a bounded wait on an mbarrier ran out */
+#define LOCKS_FLAG_BAD_SELECT  8u  /* a selected index outside [0, n_b) was skipped */
+
+/* Bytes of one page-head summary record (784 for the supported shape),
+ * 0 for an unsupported cfg. */
+size_t locks_summary_bytes(const locks_cfg *cfg);
+
+/* Workspace bytes needed by score/select and sparse/dense decode for this
+ * batch shape (one workspace may be shared by all calls of a step, used in
+ * stream order).  Host only, no CUDA call. */
+locks_status locks_workspace_bytes(const locks_cfg *cfg, int32_t batch, int32_t max_pages,
+                                   int32_t budget_pages, size_t *bytes);
+
+/* Zero a workspace before its first use (the status word and the merge
+ * tickets must start at zero; the kernels keep the tickets at zero after
+ * every call).  Enqueues one memset on `stream`. */
+locks_status locks_workspace_init(void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* Synchronise `stream`, copy the status word to *flags and clear it. */
+locks_status locks_read_status(void *workspace, uint32_t *flags, locks_stream_t stream);
+
+/* Page summary builder, §2 "page-local spectral decomposition" and
+ * "quantisation": for each of the n_build physical blocks in block_ids
+ * (device int32) and each KV head, read the 16 keys of k_cache and write the
+ * 784-byte record described above into `summaries`.  Meant to run when pages
+ * are finalised (prefill, or a page crossing), off the decode critical path.
+ * Block ids outside [0, num_blocks) are skipped and flagged.  Uses only the
+ * status word of `workspace` (workspace may be NULL: no flag is reported). */
+locks_status locks_build_summaries(const locks_cfg *cfg, const void *k_cache, int64_t num_blocks,
+                                   const int32_t *block_ids, int32_t n_build, void *summaries,
+                                   void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* Scoring pass, §2 "reconstruction and selection" (the s_j(q) equation):
+ * for every request b, KV head h and full page j < n_b, read the page's
+ * record (and nothing else of the cache) and write, for each query head g of
+ * the group, s_j = log sum_i exp((q.mu_j + (V_j^T q).c_i) / sqrt(d)) into
+ * `scores` (or into the workspace when scores is NULL), plus per-chunk
+ * partial log-sum-exps that locks_select combines. */
+locks_status locks_score(const locks_cfg *cfg, const void *q, const void *summaries,
+                         int64_t num_blocks, const int32_t *block_table, const int32_t *seq_lens,
+                         int32_t batch, int32_t max_pages, float *scores,
+                         void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* Selection pass, §2 "reconstruction and selection" and "group-shared
+ * selection (GQA)": Z_{b,h,g} = logsumexp over full pages of s_j; share =
+ * exp(s_j - Z); the group's table is the mean share over its G query heads;
+ * the min(budget_pages, n_b) largest entries (lower page index on ties) are
+ * written to selected[b][h][...] in ascending page order and their count to
+ * n_selected[b][h].  `scores` must be what locks_score was given. */
+locks_status locks_select(const locks_cfg *cfg, const int32_t *seq_lens, int32_t batch,
+                          int32_t max_pages, int32_t budget_pages, const float *scores,
+                          int32_t *selected, int32_t *n_selected,
+                          void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* locks_score followed by locks_select on the same stream. */
+locks_status locks_score_select(const locks_cfg *cfg, const void *q, const void *summaries,
+                                int64_t num_blocks, const int32_t *block_table,
+                                const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                                int32_t budget_pages, float *scores, int32_t *selected,
+                                int32_t *n_selected, void *workspace, size_t workspace_bytes,
+                                locks_stream_t stream);
+
+/* Sparse paged decode attention, §2 / abstract "attends only the top pages":
+ * for each (b, h) and each of the G query heads of the group,
+ * out = softmax(sm_scale * q K^T) V over the tokens of the selected full
+ * pages plus the t_b tokens of the open tail page (always attended).  All G
+ * heads share each K/V page read.  Split-K over pages with an online-softmax
+ * merge.  sm_scale is normally 1/sqrt(128). */
+locks_status locks_sparse_decode(const locks_cfg *cfg, const void *q, const void *k_cache,
+                                 const void *v_cache, int64_t num_blocks,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 const int32_t *selected, const int32_t *n_selected,
+                                 int32_t batch, int32_t max_pages, int32_t budget_pages,
+                                 float sm_scale, float *out, void *workspace,
+                                 size_t workspace_bytes, locks_stream_t stream);
+
+/* Dense comparator (the full-cache attention LOCKS is measured against):
+ * the same computation over every cached token of each request. */
+locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void *k_cache,
+                                const void *v_cache, int64_t num_blocks,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                int32_t batch, int32_t max_pages, float sm_scale, float *out,
+                                void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* Static description of a status code. */
+const char *locks_status_str(locks_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOCKS_H */

@@ -1,0 +1,364 @@
+// api.cu -- extern "C" entry points of liblocks (declared in include/locks.h).
+//
+// Host side only: argument validation (before any launch), work planning
+// (grid shapes and workspace regions, a pure function of the batch shape so
+// that locks_workspace_bytes and every launch agree), tensor-map encoding for
+// the attention kernel, and launches.  No allocation, no synchronisation on
+// the decode path.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/locks.h"
+#include "common.cuh"
+
+#include "params.h"
+
+namespace {
+
+using namespace locks;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  // scoring
+  int h_cta, wph, pps, head_groups, ch_pages, n_chunks, n_items, score_grid;
+  // attention
+  int sparse_splits, sparse_ips, dense_splits, dense_ips, max_splits;
+  // workspace regions
+  size_t off_partials, off_scores, off_keys, off_attn, off_tickets, total;
+};
+
+bool cfg_supported(const locks_cfg* c) {
+  if (c == nullptr) return false;
+  if (c->head_dim != kHeadDim || c->page_size != kPage || c->rank != kRank) return false;
+  if (c->quant != 1 || c->group_size != kGroup) return false;
+  const int H = c->num_kv_heads;
+  if (H < 1) return false;
+  const int h_cta = H < 8 ? H : 8;
+  return (8 % h_cta == 0) && (H % h_cta == 0);
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+int pick_splits(int units, int max_items) {
+  // aim for ~8 waves of resident CTAs, at least 4 items (one per warp) each
+  const int by_items = max(1, ceil_div(max_items, 4));
+  const int want = max(1, ceil_div(8 * kTargetCtas, units));
+  return max(1, min(by_items, want));
+}
+
+Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
+  Plan pl{};
+  const int H = c->num_kv_heads;
+  pl.h_cta = H < 8 ? H : 8;
+  pl.wph = 8 / pl.h_cta;
+  pl.pps = 4 * pl.wph;
+  pl.head_groups = H / pl.h_cta;
+  pl.ch_pages = 8 * pl.pps;
+  pl.n_chunks = ceil_div(max_pages, pl.ch_pages);
+  const int64_t items = (int64_t)batch * pl.head_groups * pl.n_chunks;
+  pl.n_items = (int)items;
+  pl.score_grid = (int)(items < kTargetCtas ? items : kTargetCtas);
+  const int units = batch * H;
+  pl.sparse_splits = pick_splits(units, budget + 1);
+  pl.sparse_ips = ceil_div(budget + 1, pl.sparse_splits);
+  pl.dense_splits = pick_splits(units, max_pages);
+  pl.dense_ips = ceil_div(max_pages, pl.dense_splits);
+  pl.max_splits = max(pl.sparse_splits, pl.dense_splits);
+
+  size_t off = kAlign;  // [0, 256): status word
+  pl.off_partials = off;
+  off = align_up(off + (size_t)batch * H * pl.n_chunks * pl.wph * kGroup * 2 * sizeof(float));
+  pl.off_scores = off;
+  off = align_up(off + (size_t)batch * H * max_pages * kGroup * sizeof(float));
+  pl.off_keys = off;
+  off = align_up(off + (size_t)batch * H * max_pages * sizeof(uint32_t));
+  pl.off_attn = off;
+  off = align_up(off + (size_t)units * pl.max_splits * kGroup * (2 + kHeadDim) * sizeof(float));
+  pl.off_tickets = off;
+  off = align_up(off + (size_t)units * sizeof(uint32_t));
+  pl.total = off;
+  return pl;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define LOCKS_CHECK_PTR(p) \
+  do {                     \
+    if ((p) == nullptr || !aligned16(p)) return LOCKS_ERR_INVALID_ARG; \
+  } while (0)
+
+uint32_t* status_word(void* ws) { return ws ? reinterpret_cast<uint32_t*>(ws) : nullptr; }
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view of a [num_blocks][H][16][128] bf16 cache: rows = page-head tokens,
+// 128 columns; boxes of 16 rows x 64 columns with 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int H) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(num_blocks * H * kPage)};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, kPage};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+locks_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
+
+locks_status attention_common(const locks_cfg* cfg, const void* q, const void* k_cache,
+                              const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                              const int32_t* seq_lens, const int32_t* selected,
+                              const int32_t* n_selected, int32_t batch, int32_t max_pages,
+                              int32_t budget_pages, float sm_scale, float* out, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream, bool dense) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || sm_scale != sm_scale) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(q);
+  LOCKS_CHECK_PTR(k_cache);
+  LOCKS_CHECK_PTR(v_cache);
+  LOCKS_CHECK_PTR(block_table);
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(out);
+  LOCKS_CHECK_PTR(workspace);
+  if (!dense) {
+    LOCKS_CHECK_PTR(n_selected);
+    if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+  }
+  const int H = cfg->num_kv_heads;
+  if (num_blocks * H * kPage >= (int64_t)1 << 31) return LOCKS_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
+  if (ws_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+
+  CUtensorMap tmk, tmv;
+  if (!encode_cache_map(&tmk, k_cache, num_blocks, H) || !encode_cache_map(&tmv, v_cache, num_blocks, H))
+    return LOCKS_ERR_CUDA;
+
+  AttnParams p{};
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.selected = selected;
+  p.n_selected = n_selected;
+  p.out = out;
+  p.part = reinterpret_cast<float*>(ws + pl.off_attn);
+  p.tickets = reinterpret_cast<uint32_t*>(ws + pl.off_tickets);
+  p.status = status_word(workspace);
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.max_pages = max_pages;
+  p.H_kv = H;
+  p.budget = budget_pages;
+  p.dense = dense ? 1 : 0;
+  p.splits = dense ? pl.dense_splits : pl.sparse_splits;
+  p.items_per_split = dense ? pl.dense_ips : pl.sparse_ips;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  return from_cuda(launch_attn(tmk, tmv, p, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t locks_summary_bytes(const locks_cfg* cfg) { return cfg_supported(cfg) ? (size_t)kRecord : 0; }
+
+locks_status locks_workspace_bytes(const locks_cfg* cfg, int32_t batch, int32_t max_pages,
+                                   int32_t budget_pages, size_t* bytes) {
+  if (cfg == nullptr || bytes == nullptr) return LOCKS_ERR_INVALID_ARG;
+  if (!cfg_supported(cfg)) return LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0) return LOCKS_ERR_INVALID_ARG;
+  *bytes = make_plan(cfg, batch, max_pages, budget_pages).total;
+  return LOCKS_OK;
+}
+
+locks_status locks_workspace_init(void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < kAlign) return LOCKS_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_read_status(void* workspace, uint32_t* flags, locks_stream_t stream) {
+  if (workspace == nullptr || flags == nullptr) return LOCKS_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return LOCKS_ERR_CUDA;
+  *flags = v;
+  return LOCKS_OK;
+}
+
+locks_status locks_build_summaries(const locks_cfg* cfg, const void* k_cache, int64_t num_blocks,
+                                   const int32_t* block_ids, int32_t n_build, void* summaries,
+                                   void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (n_build < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
+  if (n_build == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(k_cache);
+  LOCKS_CHECK_PTR(block_ids);
+  LOCKS_CHECK_PTR(summaries);
+  if (workspace != nullptr && (!aligned16(workspace) || workspace_bytes < sizeof(uint32_t)))
+    return LOCKS_ERR_INVALID_ARG;
+  BuildParams p{};
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.block_ids = block_ids;
+  p.summ = static_cast<uint8_t*>(summaries);
+  p.status = status_word(workspace);
+  p.num_blocks = num_blocks;
+  p.n_build = n_build;
+  p.H_kv = cfg->num_kv_heads;
+  return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summaries, int64_t num_blocks,
+                         const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                         int32_t max_pages, float* scores, void* workspace, size_t workspace_bytes,
+                         locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(q);
+  LOCKS_CHECK_PTR(summaries);
+  LOCKS_CHECK_PTR(block_table);
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(workspace);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  const Plan pl = make_plan(cfg, batch, max_pages, 0);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ScoreParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.summ = static_cast<const uint8_t*>(summaries);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.scores = scores ? scores : reinterpret_cast<float*>(ws + pl.off_scores);
+  p.partials = reinterpret_cast<float*>(ws + pl.off_partials);
+  p.status = status_word(workspace);
+  p.num_blocks = num_blocks;
+  p.batch = batch;
+  p.max_pages = max_pages;
+  p.H_kv = cfg->num_kv_heads;
+  p.h_cta = pl.h_cta;
+  p.wph = pl.wph;
+  p.pps = pl.pps;
+  p.ch_pages = pl.ch_pages;
+  p.n_chunks = pl.n_chunks;
+  p.head_groups = pl.head_groups;
+  p.n_items = pl.n_items;
+  return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                          int32_t budget_pages, const float* scores, int32_t* selected,
+                          int32_t* n_selected, void* workspace, size_t workspace_bytes,
+                          locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(n_selected);
+  LOCKS_CHECK_PTR(workspace);
+  if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SelectParams p{};
+  p.seq_lens = seq_lens;
+  p.scores = scores ? scores : reinterpret_cast<const float*>(ws + pl.off_scores);
+  p.partials = reinterpret_cast<const float*>(ws + pl.off_partials);
+  p.keys = reinterpret_cast<uint32_t*>(ws + pl.off_keys);
+  p.selected = selected;
+  p.n_selected = n_selected;
+  p.status = status_word(workspace);
+  p.batch = batch;
+  p.max_pages = max_pages;
+  p.H_kv = cfg->num_kv_heads;
+  p.budget = budget_pages;
+  p.n_chunks = pl.n_chunks;
+  p.wph = pl.wph;
+  return from_cuda(launch_select(p, batch * cfg->num_kv_heads, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_score_select(const locks_cfg* cfg, const void* q, const void* summaries,
+                                int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_pages, int32_t budget_pages, float* scores,
+                                int32_t* selected, int32_t* n_selected, void* workspace,
+                                size_t workspace_bytes, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (budget_pages < 0) return LOCKS_ERR_INVALID_ARG;
+  if (batch > 0) {
+    LOCKS_CHECK_PTR(n_selected);
+    if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+  }
+  locks_status st = locks_score(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages,
+                                scores, workspace, workspace_bytes, stream);
+  if (st != LOCKS_OK) return st;
+  return locks_select(cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected,
+                      workspace, workspace_bytes, stream);
+}
+
+locks_status locks_sparse_decode(const locks_cfg* cfg, const void* q, const void* k_cache,
+                                 const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                                 const int32_t* seq_lens, const int32_t* selected,
+                                 const int32_t* n_selected, int32_t batch, int32_t max_pages,
+                                 int32_t budget_pages, float sm_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, locks_stream_t stream) {
+  return attention_common(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, selected, n_selected,
+                          batch, max_pages, budget_pages, sm_scale, out, workspace, workspace_bytes,
+                          reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+locks_status locks_dense_decode(const locks_cfg* cfg, const void* q, const void* k_cache,
+                                const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                                const int32_t* seq_lens, int32_t batch, int32_t max_pages, float sm_scale,
+                                float* out, void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  return attention_common(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, nullptr, nullptr,
+                          batch, max_pages, 0, sm_scale, out, workspace, workspace_bytes,
+                          reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+const char* locks_status_str(locks_status s) {
+  switch (s) {
+    case LOCKS_OK: return "ok";
+    case LOCKS_ERR_INVALID_ARG: return "invalid argument";
+    case LOCKS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LOCKS_ERR_WORKSPACE: return "workspace too small";
+    case LOCKS_ERR_CUDA: return "CUDA error";
+    case LOCKS_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,371 @@
+// build_summaries.cu -- LOCKS page summary builder (a1) with quantisation (a2).
+//
+// "LOCKS: Page-Local Compact Key Summaries for Efficient Long-Context
+// Decoding", technical summary §2, "page-local spectral decomposition": when a
+// page is finalised its keys are centred on the page centroid, a small
+// eigendecomposition of the deviations is taken, and the top-r eigenvectors
+// (the page's own basis) plus per-token coefficients are kept; "quantisation":
+// basis in int4, coefficients and centroid in int8 (about 10 % of the page's
+// KV bytes at B = 16, r = 8).  Built off the decode critical path.
+//
+// One half-warp per page-head (two per warp, four warps per CTA):
+//   1. lane i loads 16-byte chunk i of every key row (coalesced), forms the
+//      centroid of its 8 dims and writes the centred rows X to shared memory;
+//   2. lane i computes row i of the Gram matrix G = X X^T (16 x 16, fp32);
+//   3. parallel cyclic Jacobi (round-robin pairing, 8 disjoint rotations per
+//      round, 15 rounds per sweep) with lane i owning row i of G and of the
+//      eigenvector matrix W; sweeps stop when the off-diagonal mass is below
+//      1e-12 of the total (at most kMaxSweeps);
+//   4. eigenvalues ranked (descending, lower index on ties), top 8 kept,
+//      sign fixed so the largest |coefficient| of each direction is positive,
+//      lambda_k <= 1e-6 lambda_1 -> zero direction;
+//   5. V = X^T W_r Lambda^{-1/2} (lane i: dims 8i..8i+7), C = W_r Lambda^{1/2};
+//   6. symmetric per-tensor quantisation (round half to even) and packing into
+//      the 784-byte record, stored with 16-byte writes.
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "params.h"
+
+namespace locks {
+
+constexpr int kBuildWarps = 4;
+constexpr int kBuildThreads = kBuildWarps * 32;
+constexpr int kXStride = 132;          // padded fp32 row of X (conflict-free LDS.128)
+constexpr int kMaxSweeps = 12;
+
+struct HalfWarpSmem {
+  float X[kPage * kXStride];           // centred keys
+  float G[kPage * kPage];              // current Gram rows (for diagonal reads)
+  float W[kPage * kPage];              // eigenvectors (rows)
+  float2 rot[kPage];                   // (c, s) of the pair containing index j
+  float lift[kPage * kRank];           // W_r Lambda^{-1/2} (signed)
+  float coef[kPage * kRank];           // C
+  int order[kPage];
+  int8_t vcode[kRank * kHeadDim];      // [k][dim]
+  __align__(16) uint8_t rec[kRecord];
+  float scratch[4];
+};
+constexpr int kBuildSmem = 2 * kBuildWarps * (int)sizeof(HalfWarpSmem);
+
+// Round-robin partner of index i in round r (circle method on 16 players).
+__host__ __device__ constexpr int jacobi_partner(int i, int r) {
+  return i == 15 ? r : (i == r ? 15 : (2 * r - i + 15) % 15);
+}
+
+template <int R>
+__device__ __forceinline__ void jacobi_round(float (&g)[kPage], float (&w)[kPage], int i, int hbase,
+                                             HalfWarpSmem& S) {
+  const int q = jacobi_partner(i, R);
+  const int lo = min(i, q), hi = max(i, q);
+  const float a = S.G[lo * kPage + lo];
+  const float bb = S.G[hi * kPage + hi];
+  const float e = S.G[lo * kPage + hi];
+  float c = 1.f, s = 0.f;
+  if (fabsf(e) > 1e-30f && fabsf(e) > 1e-12f * sqrtf(fabsf(a * bb))) {
+    const float tau = (bb - a) / (2.f * e);
+    const float t = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+    c = rsqrtf(1.f + t * t);
+    s = t * c;
+  }
+  S.rot[i] = make_float2(c, s);
+  // row update: rows lo, hi of J^T G
+  float pg[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) pg[j] = __shfl_sync(0xffffffffu, g[j], hbase + q);
+  const bool is_lo = (i == lo);
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) g[j] = is_lo ? (c * g[j] - s * pg[j]) : (s * pg[j] + c * g[j]);
+  __syncwarp();
+  // column update: (J^T G) J and W J; the pairing of column j is static
+  float ng[kPage], nw[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) {
+    const int pj = jacobi_partner(j, R);
+    const float2 cs = S.rot[j];
+    if (j < pj) {
+      ng[j] = cs.x * g[j] - cs.y * g[pj];
+      nw[j] = cs.x * w[j] - cs.y * w[pj];
+    } else {
+      ng[j] = cs.y * g[pj] + cs.x * g[j];
+      nw[j] = cs.y * w[pj] + cs.x * w[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) {
+    g[j] = ng[j];
+    w[j] = nw[j];
+  }
+  // publish the new row for the next round's diagonal / pivot reads
+#pragma unroll
+  for (int j = 0; j < kPage; j += 4)
+    *reinterpret_cast<float4*>(&S.G[i * kPage + j]) = make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
+  __syncwarp();
+}
+
+template <int R>
+struct Sweep {
+  static __device__ __forceinline__ void run(float (&g)[kPage], float (&w)[kPage], int i, int hbase,
+                                             HalfWarpSmem& S) {
+    jacobi_round<R>(g, w, i, hbase, S);
+    Sweep<R + 1>::run(g, w, i, hbase, S);
+  }
+};
+template <>
+struct Sweep<15> {
+  static __device__ __forceinline__ void run(float (&)[kPage], float (&)[kPage], int, int, HalfWarpSmem&) {}
+};
+
+__global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams p) {
+  extern __shared__ __align__(16) uint8_t smem_b[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, i = lane & 15, hbase = lane & 16;
+  HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_b)[warp * 2 + half];
+
+  const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;   // page-head index
+  const int64_t total = (int64_t)p.n_build * p.H_kv;
+  bool active = ph < total;
+  int64_t blk = -1;
+  int h = 0;
+  if (active) {
+    blk = p.block_ids[ph / p.H_kv];
+    h = (int)(ph % p.H_kv);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+      active = false;
+    }
+  }
+  // Both half-warps run every step (warp-synchronous shuffles); an inactive
+  // half works on a zero page and stores nothing.
+
+  // ---- 1. load, centroid, centred rows
+  float mu8[8];
+  {
+    float kv[kPage][8];
+    const __nv_bfloat16* src = p.k_cache + ((active ? blk : 0) * p.H_kv + h) * (int64_t)(kPage * kHeadDim);
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (active) raw = *reinterpret_cast<const uint4*>(src + r * kHeadDim + 8 * i);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kv[r][2 * e] = __low2float(b2[e]);
+        kv[r][2 * e + 1] = __high2float(b2[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float sum = 0.f;
+#pragma unroll
+      for (int r = 0; r < kPage; ++r) sum += kv[r][e];
+      mu8[e] = sum * (1.f / kPage);
+    }
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      float* xr = &S.X[r * kXStride + 8 * i];
+      *reinterpret_cast<float4*>(xr) = make_float4(kv[r][0] - mu8[0], kv[r][1] - mu8[1], kv[r][2] - mu8[2], kv[r][3] - mu8[3]);
+      *reinterpret_cast<float4*>(xr + 4) = make_float4(kv[r][4] - mu8[4], kv[r][5] - mu8[5], kv[r][6] - mu8[6], kv[r][7] - mu8[7]);
+    }
+  }
+  __syncwarp();
+
+  // ---- 2. Gram row i
+  float g[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) g[j] = 0.f;
+  for (int d = 0; d < kHeadDim; d += 4) {
+    const float4 xi = *reinterpret_cast<const float4*>(&S.X[i * kXStride + d]);
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) {
+      const float4 xj = *reinterpret_cast<const float4*>(&S.X[j * kXStride + d]);
+      g[j] = fmaf(xi.x, xj.x, g[j]);
+      g[j] = fmaf(xi.y, xj.y, g[j]);
+      g[j] = fmaf(xi.z, xj.z, g[j]);
+      g[j] = fmaf(xi.w, xj.w, g[j]);
+    }
+  }
+  float w[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) w[j] = (j == i) ? 1.f : 0.f;
+#pragma unroll
+  for (int j = 0; j < kPage; j += 4)
+    *reinterpret_cast<float4*>(&S.G[i * kPage + j]) = make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
+  __syncwarp();
+
+  // ---- 3. Jacobi sweeps
+  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
+    float tot = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) tot = fmaf(g[j], g[j], tot);
+    const float dii = S.G[i * kPage + i];
+    float off = tot - dii * dii;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      off += __shfl_xor_sync(0xffffffffu, off, o);
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    }
+    const bool done = !(off > 1e-12f * tot);
+    if (__all_sync(0xffffffffu, done)) break;
+    Sweep<0>::run(g, w, i, hbase, S);
+  }
+
+  // ---- 4. rank eigenvalues, pick the top r, fix signs
+#pragma unroll
+  for (int j = 0; j < kPage; j += 4)
+    *reinterpret_cast<float4*>(&S.W[i * kPage + j]) = make_float4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+  __syncwarp();
+  float lam[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) lam[j] = S.G[j * kPage + j];
+  const float my_lam = lam[i];
+  int rank = 0;
+  float lam1 = lam[0];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) {
+    rank += (lam[j] > my_lam) || (lam[j] == my_lam && j < i);
+    lam1 = fmaxf(lam1, lam[j]);
+  }
+  S.order[rank] = i;
+  float tail = rank >= kRank ? fmaxf(my_lam, 0.f) : 0.f;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) tail += __shfl_xor_sync(0xffffffffu, tail, o);
+  __syncwarp();
+  if (i < kRank) {
+    const int ev = S.order[i];
+    const float l = S.G[ev * kPage + ev];
+    const bool keep = l > 1e-6f * lam1 && l > 0.f;
+    // sign: largest |component| of this eigenvector positive (first on ties)
+    float best = -1.f, sgn = 1.f;
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      const float v = S.W[r * kPage + ev];
+      if (fabsf(v) > best) {
+        best = fabsf(v);
+        sgn = v < 0.f ? -1.f : 1.f;
+      }
+    }
+    const float sig = keep ? sqrtf(l) : 0.f;
+    const float inv = keep ? 1.f / sig : 0.f;
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      const float v = S.W[r * kPage + ev] * sgn;
+      S.lift[r * kRank + i] = v * inv;
+      S.coef[r * kRank + i] = v * sig;
+    }
+  }
+  __syncwarp();
+
+  // ---- 5. V = X^T W_r Lambda^{-1/2}: lane i -> dims 8i..8i+7
+  float V[8][kRank];
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int k = 0; k < kRank; ++k) V[e][k] = 0.f;
+#pragma unroll 4
+  for (int r = 0; r < kPage; ++r) {
+    const float4 x0 = *reinterpret_cast<const float4*>(&S.X[r * kXStride + 8 * i]);
+    const float4 x1 = *reinterpret_cast<const float4*>(&S.X[r * kXStride + 8 * i + 4]);
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const float4 l0 = *reinterpret_cast<const float4*>(&S.lift[r * kRank]);
+    const float4 l1 = *reinterpret_cast<const float4*>(&S.lift[r * kRank + 4]);
+    const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int k = 0; k < kRank; ++k) V[e][k] = fmaf(xs[e], ls[k], V[e][k]);
+  }
+
+  // ---- 6. quantise and pack
+  float vmax = 0.f, mmax = 0.f, cmax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mmax = fmaxf(mmax, fabsf(mu8[e]));
+#pragma unroll
+    for (int k = 0; k < kRank; ++k) vmax = fmaxf(vmax, fabsf(V[e][k]));
+  }
+  float crow[kRank];
+#pragma unroll
+  for (int k = 0; k < kRank; ++k) {
+    crow[k] = S.coef[i * kRank + k];
+    cmax = fmaxf(cmax, fabsf(crow[k]));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+  }
+  const float sV = vmax / 7.f, sM = mmax / 127.f, sC = cmax / 127.f;
+  // V codes -> [k][dim] bytes
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+#pragma unroll
+    for (int k = 0; k < kRank; ++k) {
+      int c = sV > 0.f ? __float2int_rn(__fdiv_rn(V[e][k], sV)) : 0;
+      c = max(-7, min(7, c));
+      S.vcode[k * kHeadDim + 8 * i + e] = (int8_t)c;
+    }
+  // centroid codes straight into the record
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int dim = 8 * i + e;
+    int c = sM > 0.f ? __float2int_rn(__fdiv_rn(mu8[e], sM)) : 0;
+    c = max(-127, min(127, c));
+    const int s = dim >> 4, wd = dim & 15, hh = wd >> 3, t = (wd & 7) >> 1, ee = wd & 1;
+    S.rec[512 + t * 32 + s * 4 + hh * 2 + ee] = (uint8_t)(int8_t)c;
+  }
+  // coefficient codes of token i
+#pragma unroll
+  for (int k = 0; k < kRank; ++k) {
+    int c = sC > 0.f ? __float2int_rn(__fdiv_rn(crow[k], sC)) : 0;
+    c = max(-127, min(127, c));
+    const int nt = i >> 3, gd = i & 7, tk = k >> 1, ek = k & 1;
+    S.rec[640 + (gd * 4 + tk) * 4 + nt * 2 + ek] = (uint8_t)(int8_t)c;
+  }
+  if (i == 0) {
+    float* scl = reinterpret_cast<float*>(&S.rec[768]);
+    scl[0] = sV;
+    scl[1] = sM;
+    scl[2] = sC;
+    scl[3] = tail;
+  }
+  __syncwarp();
+  // pack basis words: lane i builds words i, i+16, ..., i+112 (word = k*16 + t*4 + p)
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int wi = i + 16 * m;
+    const int k = wi >> 4, t = (wi >> 2) & 3, pp = wi & 3;
+    uint32_t word = 0;
+#pragma unroll
+    for (int pos = 0; pos < 8; ++pos) {
+      const int e = pos >> 2, sp = (pos & 3) >> 1, hh = pos & 1;
+      const int dim = 16 * (2 * pp + sp) + 8 * hh + 2 * t + e;
+      word |= ((uint32_t)S.vcode[k * kHeadDim + dim] & 0xFu) << (4 * pos);
+    }
+    *reinterpret_cast<uint32_t*>(&S.rec[k * 64 + t * 16 + pp * 4]) = word;
+  }
+  __syncwarp();
+  if (active) {
+    uint4* dst = reinterpret_cast<uint4*>(p.summ + (blk * p.H_kv + h) * (int64_t)kRecord);
+    const uint4* srcr = reinterpret_cast<const uint4*>(S.rec);
+    for (int c = i; c < kRecord / 16; c += 16) dst[c] = srcr[c];
+  }
+}
+
+cudaError_t launch_build(const BuildParams& p, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t page_heads = (int64_t)p.n_build * p.H_kv;
+  const int64_t grid = (page_heads + 2 * kBuildWarps - 1) / (2 * kBuildWarps);
+  if (grid == 0) return cudaSuccess;
+  build_kernel<<<(unsigned)grid, kBuildThreads, kBuildSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace locks

@@ -1,0 +1,374 @@
+// decode_attention.cu -- split-K paged decode attention for LOCKS (a6) and the
+// dense comparator (a7).
+//
+// "LOCKS: Page-Local Compact Key Summaries for Efficient Long-Context
+// Decoding", abstract and technical summary §2: after selection only the top
+// pages are attended, with all query heads of a GQA group attending the same
+// pages (so one K/V read serves the whole group).  The still-open tail page
+// (no summary yet) is always attended.  The dense comparator is the same
+// kernel over every cached page.
+//
+// Grid: (split, request x KV head).  Each CTA owns a contiguous slice of the
+// unit's item list (selected pages + tail, or all pages + tail); each of its 4
+// warps runs its own 3-stage ring: lane 0 issues four 2 KB cp.async.bulk.tensor
+// loads per page (K and V, 64-column halves, 128-byte swizzle) onto an
+// mbarrier, the warp waits, then
+//   S = K q^T   (mma.sync m16n8k16 bf16: 16 tokens x 8 columns (4 heads, padded))
+//   online softmax per head (exp2, running max / sum)
+//   O^T += V^T P (ldmatrix.trans on the swizzled V tile; P transposed in
+//                 registers with movmatrix)
+// Warps merge through shared memory; splits merge through per-split partials
+// in the workspace, combined by the last CTA of each unit (atomic ticket, no
+// spinning).
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "params.h"
+
+namespace locks {
+
+
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kAttnStages = 3;
+constexpr int kTileBytes = kPage * kHeadDim * 2;           // 4096: one page-head of K (or V)
+constexpr int kStageBytes = 2 * kTileBytes;                // K + V
+constexpr int kAttnRing = kAttnWarps * kAttnStages * kStageBytes;
+constexpr int kAttnSmem = kAttnRing + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kPartStride = 2 + kHeadDim;
+
+// Swizzled (128B) address of 16-byte chunk `chunk` (0..15 across the 128
+// columns) of row `row` of a K/V tile made of two 64-column boxes.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int row, int chunk) {
+  const int half = chunk >> 3, c = chunk & 7;
+  return tile + half * 2048 + row * 128 + ((c ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void unit_items(const AttnParams& p, int b, int h, int& n, int& t,
+                                           int& nsel, int& items) {
+  const int L = p.seq_lens[b];
+  if (L < 0 || (L + kPage - 1) / kPage > p.max_pages) {
+    n = t = nsel = items = 0;
+    return;
+  }
+  n = L / kPage;
+  t = L % kPage;
+  if (p.dense) {
+    nsel = n;
+  } else {
+    nsel = p.n_selected[b * p.H_kv + h];
+    const int cap = min(p.budget, n);
+    if (nsel < 0 || nsel > cap) nsel = max(0, min(nsel, cap));
+  }
+  items = nsel + (t > 0 ? 1 : 0);
+}
+
+// Resolve item i of the unit: physical block (or -1 to skip) and valid tokens.
+__device__ __forceinline__ void item_block(const AttnParams& p, int b, int h, int i, int n, int t,
+                                           int nsel, int64_t& blk, int& valid) {
+  int page;
+  if (i < nsel) {
+    page = p.dense ? i : p.selected[((int64_t)b * p.H_kv + h) * p.budget + i];
+    valid = kPage;
+    if (page < 0 || page >= n) {
+      flag_status(p.status, LOCKS_FLAG_BAD_SELECT);
+      blk = -1;
+      valid = 0;
+      return;
+    }
+  } else {
+    page = n;
+    valid = t;
+  }
+  blk = p.block_table[(int64_t)b * p.max_pages + page];
+  if (blk < 0 || blk >= p.num_blocks) {
+    flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+    blk = -1;
+    valid = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 2)
+    attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kAttnRing);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, t4 = lane & 3;
+  const int unit = blockIdx.y, split = blockIdx.x;
+  const int b = unit / p.H_kv, h = unit % p.H_kv;
+
+  int n, tail, nsel, items;
+  unit_items(p, b, h, n, tail, nsel, items);
+  const int r0 = min(items, split * p.items_per_split);
+  const int r1 = min(items, r0 + p.items_per_split);
+  // this warp's items: r0 + warp, r0 + warp + 4, ...
+  const int my_first = r0 + warp;
+  const int my_count = my_first < r1 ? (r1 - my_first + kAttnWarps - 1) / kAttnWarps : 0;
+
+  uint64_t* mybar = bars + warp * kAttnStages;
+  const uint32_t ring = smem_u32(smem) + warp * kAttnStages * kStageBytes;
+  uint8_t* ring_ptr = smem + warp * kAttnStages * kStageBytes;
+  if (lane == 0) {
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(&mybar[s], 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  __syncwarp();
+
+  // Item metadata windows: lane l of `cur` describes issue index base + l,
+  // `nxt` the 32 after it (loaded one window ahead so refills never wait).
+  __shared__ int stage_valid[kAttnWarps][kAttnStages];
+  int64_t cur_blk = -1, nxt_blk = -1;
+  int cur_valid = 0, nxt_valid = 0;
+  if (lane < my_count)
+    item_block(p, b, h, my_first + lane * kAttnWarps, n, tail, nsel, cur_blk, cur_valid);
+  if (32 + lane < my_count)
+    item_block(p, b, h, my_first + (32 + lane) * kAttnWarps, n, tail, nsel, nxt_blk, nxt_valid);
+
+  auto issue = [&](int64_t blk, int stage) {
+    uint64_t* bar = &mybar[stage];
+    uint8_t* dst = ring_ptr + stage * kStageBytes;
+    if (blk >= 0) {
+      mbar_arrive_expect_tx(bar, kStageBytes);
+      const int32_t y = (int32_t)((blk * p.H_kv + h) * kPage);
+      tma_load_2d(dst, &tmk, 0, y, bar);
+      tma_load_2d(dst + 2048, &tmk, 64, y, bar);
+      tma_load_2d(dst + kTileBytes, &tmv, 0, y, bar);
+      tma_load_2d(dst + kTileBytes + 2048, &tmv, 64, y, bar);
+    } else {
+      mbar_arrive(bar);   // nothing to load: complete the phase at once
+    }
+  };
+
+  // prologue: lane k issues item k into stage k
+  if (lane < min(kAttnStages, my_count)) {
+    stage_valid[warp][lane] = cur_valid;
+    issue(cur_blk, lane);
+  }
+
+  // B operand of S = K q^T: column n = head n & 3 of the group.
+  uint32_t qb[8][2];
+  {
+    const __nv_bfloat16* qh = p.q + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup + (gid & 3)) * kHeadDim;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      qb[s][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * t4);
+      qb[s][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * t4 + 8);
+    }
+  }
+  __syncwarp();
+
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  bool ok = true;
+
+  for (int k = 0; k < my_count; ++k) {
+    const int stage = k % kAttnStages;
+    if (ok) ok = mbar_wait(&mybar[stage], (k / kAttnStages) & 1, p.status);
+    const int valid = stage_valid[warp][stage];
+    const uint32_t ktile = ring + stage * kStageBytes;
+    const uint32_t vtile = ktile + kTileBytes;
+
+    if (ok && valid > 0) {
+      if (valid < kPage) {
+        // tail page: zero the V rows past the valid tokens (they may hold
+        // anything, and 0 * NaN would poison the accumulator)
+        uint8_t* vp = ring_ptr + stage * kStageBytes + kTileBytes;
+        for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
+          const int row = valid + idx / 16, chunk = idx % 16;
+          const int half = chunk >> 3, c = chunk & 7;
+          *reinterpret_cast<uint4*>(vp + half * 2048 + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // ---- S = K q^T (rows = tokens, cols = heads)
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int lchk = lane >> 4;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, tile_addr(ktile, lrow, 2 * ks + lchk));
+        mma_bf16(s, a[0], a[1], a[2], a[3], qb[ks][0], qb[ks][1]);
+      }
+      // scale into log2 units, mask invalid tokens
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[i] *= p.scale_log2;
+      if (gid >= valid) s[0] = s[1] = -INFINITY;
+      if (gid + 8 >= valid) s[2] = s[3] = -INFINITY;
+      // ---- online softmax, per column (2t4, 2t4+1)
+      float mt0 = fmaxf(s[0], s[2]), mt1 = fmaxf(s[1], s[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], mt0), mn1 = fmaxf(m_run[1], mt1);
+      const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+      const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
+      const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
+      l_run[0] = l_run[0] * al0 + p0 + p2;
+      l_run[1] = l_run[1] * al1 + p1 + p3;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i][0] *= al0;
+        acc[i][1] *= al1;
+        acc[i][2] *= al0;
+        acc[i][3] *= al1;
+      }
+      // P^T as the B operand (k = tokens, n = heads)
+      const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+      const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+      // ---- O^T[dim][head] += V^T P
+      const int vrow = (lane & 7) + (lane >> 4) * 8;
+      const int vsel = (lane >> 3) & 1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, tile_addr(vtile, vrow, 2 * i + vsel));
+        mma_bf16(acc[i], a[0], a[1], a[2], a[3], pb0, pb1);
+      }
+    }
+    // order this warp's generic smem accesses before the next async write
+    fence_proxy_async_smem();
+    __syncwarp();
+    // refill this stage with item k + S
+    const int kn = k + kAttnStages;
+    if (kn < my_count) {
+      if ((kn & 31) == 0) {
+        cur_blk = nxt_blk;
+        cur_valid = nxt_valid;
+        nxt_blk = -1;
+        nxt_valid = 0;
+        if (kn + 32 + lane < my_count)
+          item_block(p, b, h, my_first + (kn + 32 + lane) * kAttnWarps, n, tail, nsel, nxt_blk, nxt_valid);
+      }
+      const int64_t blk = __shfl_sync(0xffffffffu, cur_blk, kn & 31);
+      const int v = __shfl_sync(0xffffffffu, cur_valid, kn & 31);
+      if (lane == 0) {
+        stage_valid[warp][stage] = v;
+        issue(blk, stage);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- reduce l over the 8 token rows (lanes with equal t4)
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
+    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
+  }
+
+  // ---- merge the 4 warps through shared memory (ring no longer in use)
+  __syncthreads();
+  float* wO = reinterpret_cast<float*>(smem);                       // [warp][G][128]
+  float* wM = wO + kAttnWarps * kGroup * kHeadDim;                  // [warp][G]
+  float* wL = wM + kAttnWarps * kGroup;                             // [warp][G]
+  if (t4 < 2) {   // columns 2t4, 2t4+1 are heads 0..3
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d0 = 16 * i + gid, d1 = d0 + 8;
+      wO[(warp * kGroup + 2 * t4) * kHeadDim + d0] = acc[i][0];
+      wO[(warp * kGroup + 2 * t4 + 1) * kHeadDim + d0] = acc[i][1];
+      wO[(warp * kGroup + 2 * t4) * kHeadDim + d1] = acc[i][2];
+      wO[(warp * kGroup + 2 * t4 + 1) * kHeadDim + d1] = acc[i][3];
+    }
+    if (gid == 0) {
+      wM[warp * kGroup + 2 * t4] = m_run[0];
+      wM[warp * kGroup + 2 * t4 + 1] = m_run[1];
+      wL[warp * kGroup + 2 * t4] = l_run[0];
+      wL[warp * kGroup + 2 * t4 + 1] = l_run[1];
+    }
+  }
+  __syncthreads();
+
+  const int d = threadIdx.x;   // 128 threads = 128 dims
+  float Mg[kGroup], Lg[kGroup], Og[kGroup];
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wM[w * kGroup + g]);
+    float Ls = 0.f, Os = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float f = fast_exp2(wM[w * kGroup + g] - M);
+        Ls += wL[w * kGroup + g] * f;
+        Os += wO[(w * kGroup + g) * kHeadDim + d] * f;
+      }
+    }
+    Mg[g] = M;
+    Lg[g] = Ls;
+    Og[g] = Os;
+  }
+
+  float* orow = p.out + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup) * kHeadDim;
+  if (p.splits == 1) {
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) orow[g * kHeadDim + d] = Lg[g] > 0.f ? Og[g] / Lg[g] : 0.f;
+    return;
+  }
+
+  float* mypart = p.part + ((int64_t)unit * p.splits + split) * kGroup * kPartStride;
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    mypart[g * kPartStride + 2 + d] = Og[g];
+    if (d == 0) {
+      mypart[g * kPartStride] = Mg[g];
+      mypart[g * kPartStride + 1] = Lg[g];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ uint32_t sh_last;
+  if (threadIdx.x == 0) {
+    const uint32_t ticket = atomicAdd(&p.tickets[unit], 1u);
+    sh_last = (ticket == (uint32_t)p.splits - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  // last CTA of the unit: combine all splits
+  const float* up = p.part + (int64_t)unit * p.splits * kGroup * kPartStride;
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(up + (sp * kGroup + g) * kPartStride));
+    float Ls = 0.f, Os = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < p.splits; ++sp) {
+        const float* q = up + (sp * kGroup + g) * kPartStride;
+        const float f = fast_exp2(__ldcg(q) - M);
+        Ls += __ldcg(q + 1) * f;
+        Os += __ldcg(q + 2 + d) * f;
+      }
+    }
+    orow[g * kHeadDim + d] = Ls > 0.f ? Os / Ls : 0.f;
+  }
+  if (threadIdx.x == 0) p.tickets[unit] = 0;   // ready for the next call
+}
+
+cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
+                        cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(p.splits, p.batch * p.H_kv);
+  attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace locks

@@ -1,0 +1,74 @@
+// params.h -- launch parameter blocks shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace locks {
+
+struct ScoreParams {
+  const __nv_bfloat16* q;
+  const uint8_t* summ;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* scores;      // [batch][H_kv][max_pages][G]
+  float* partials;    // [batch][H_kv][n_chunks][wph][G][2]
+  uint32_t* status;
+  int64_t num_blocks;
+  int batch, max_pages, H_kv;
+  int h_cta;          // KV heads per CTA (<= 8, divides 8)
+  int wph;            // warps per head = 8 / h_cta
+  int pps;            // pages per stage = 4 * wph
+  int ch_pages;       // pages per work item (chunk)
+  int n_chunks;       // chunks per (b, head group)
+  int head_groups;    // H_kv / h_cta
+  int n_items;        // batch * head_groups * n_chunks
+};
+
+struct SelectParams {
+  const int32_t* seq_lens;
+  const float* scores;
+  const float* partials;
+  uint32_t* keys;          // [batch][H_kv][max_pages]
+  int32_t* selected;       // [batch][H_kv][budget]
+  int32_t* n_selected;     // [batch][H_kv]
+  uint32_t* status;
+  int batch, max_pages, H_kv, budget, n_chunks, wph;
+};
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* selected;     // sparse only
+  const int32_t* n_selected;   // sparse only
+  float* out;
+  float* part;                 // [units][splits][G][2 + 128]
+  uint32_t* tickets;           // [units]
+  uint32_t* status;
+  int64_t num_blocks;
+  int batch, max_pages, H_kv, budget;
+  int splits, items_per_split;
+  int dense;
+  float scale_log2;            // sm_scale * log2(e)
+};
+
+struct BuildParams {
+  const __nv_bfloat16* k_cache;
+  const int32_t* block_ids;
+  uint8_t* summ;
+  uint32_t* status;
+  int64_t num_blocks;
+  int n_build, H_kv;
+};
+
+cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream);
+cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
+                        cudaStream_t stream);
+cudaError_t launch_build(const BuildParams& p, cudaStream_t stream);
+
+}  // namespace locks

@@ -1,0 +1,216 @@
+"""Thin ctypes binding of liblocks.so (declared in include/locks.h).
+
+Argument marshalling only: tensors are passed as raw device pointers, the
+current torch CUDA stream as the cudaStream_t.  Every computation happens in
+the library's kernels.  There is no fallback: if the library is missing or
+fails to load, importing the first entry point raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+from . import build as _build
+
+LOCKS_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+                3: "workspace too small", 4: "CUDA error", 5: "device wait timed out"}
+FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_TIMEOUT, FLAG_BAD_SELECT = 1, 2, 4, 8
+
+HEAD_DIM, PAGE_SIZE, RANK, GROUP = 128, 16, 8, 4
+
+
+class LocksError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} (status {status})")
+        self.status = status
+
+
+class locks_cfg(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("quant", ctypes.c_int32)]
+
+
+def make_cfg(num_kv_heads: int, group_size: int = GROUP) -> locks_cfg:
+    return locks_cfg(HEAD_DIM, PAGE_SIZE, RANK, num_kv_heads, group_size, 1)
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32, _I64, _SZ, _F = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_CFG = ctypes.POINTER(locks_cfg)
+
+_SIGS = {
+    "locks_summary_bytes": (_SZ, [_CFG]),
+    "locks_workspace_bytes": (_I32, [_CFG, _I32, _I32, _I32, ctypes.POINTER(_SZ)]),
+    "locks_workspace_init": (_I32, [_P, _SZ, _P]),
+    "locks_read_status": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "locks_build_summaries": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _SZ, _P]),
+    "locks_score": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _SZ, _P]),
+    "locks_select": (_I32, [_CFG, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "locks_score_select": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _P, _P, _P,
+                                  _P, _SZ, _P]),
+    "locks_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32, _I32,
+                                   _F, _P, _P, _SZ, _P]),
+    "locks_dense_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _I32, _F, _P, _P, _SZ,
+                                  _P]),
+    "locks_status_str": (ctypes.c_char_p, [_I32]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load liblocks.so (optionally building it first) and declare signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"liblocks.so not found at {path}; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != LOCKS_OK:
+        raise LocksError(status, where)
+
+
+# ------------------------------------------------------------------ sizes
+def locks_summary_bytes(num_kv_heads: int) -> int:
+    cfg = make_cfg(num_kv_heads)
+    return int(load().locks_summary_bytes(ctypes.byref(cfg)))
+
+
+def locks_workspace_bytes(num_kv_heads: int, batch: int, max_pages: int, budget_pages: int) -> int:
+    cfg = make_cfg(num_kv_heads)
+    out = _SZ(0)
+    _check(load().locks_workspace_bytes(ctypes.byref(cfg), batch, max_pages, budget_pages,
+                                        ctypes.byref(out)), "locks_workspace_bytes")
+    return int(out.value)
+
+
+def locks_workspace_init(workspace, stream=None) -> None:
+    _check(load().locks_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "locks_workspace_init")
+
+
+def locks_read_status(workspace, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().locks_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream)),
+           "locks_read_status")
+    return int(v.value)
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+# ------------------------------------------------------------------ calls
+def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_build_summaries(
+        ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), block_ids.numel(),
+        _ptr(summaries), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_build_summaries")
+
+
+def locks_score(num_kv_heads, q, summaries, block_table, seq_lens, workspace, scores=None,
+                stream=None):
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_score(
+        ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
+        _ptr(seq_lens), block_table.shape[0], block_table.shape[1], _ptr(scores), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "locks_score")
+
+
+def locks_select(num_kv_heads, seq_lens, max_pages, budget_pages, selected, n_selected, workspace,
+                 scores=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_select(
+        ctypes.byref(cfg), _ptr(seq_lens), seq_lens.shape[0], max_pages, budget_pages, _ptr(scores),
+        _ptr(selected), _ptr(n_selected), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_select")
+
+
+def locks_score_select(num_kv_heads, q, summaries, block_table, seq_lens, budget_pages, selected,
+                       n_selected, workspace, scores=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_score_select(
+        ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
+        _ptr(seq_lens), block_table.shape[0], block_table.shape[1], budget_pages, _ptr(scores),
+        _ptr(selected), _ptr(n_selected), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_score_select")
+
+
+def locks_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, selected,
+                        n_selected, budget_pages, out, workspace, sm_scale=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_sparse_decode(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_table), _ptr(seq_lens), _ptr(selected), _ptr(n_selected),
+        block_table.shape[0], block_table.shape[1], budget_pages, scale, _ptr(out),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_sparse_decode")
+
+
+def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, out, workspace,
+                       sm_scale=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_dense_decode(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_table), _ptr(seq_lens), block_table.shape[0], block_table.shape[1], scale,
+        _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_dense_decode")
+
+
+def locks_status_str(status: int) -> str:
+    return load().locks_status_str(status).decode()
+
+
+# ------------------------------------------------------------------ helper
+class DecodeBuffers:
+    """Device buffers of one decode step for a batch shape (allocated by torch)."""
+
+    def __init__(self, num_kv_heads: int, batch: int, max_pages: int, budget_pages: int,
+                 device="cuda"):
+        import torch
+        self.num_kv_heads, self.batch = num_kv_heads, batch
+        self.max_pages, self.budget_pages = max_pages, budget_pages
+        nbytes = locks_workspace_bytes(num_kv_heads, batch, max_pages, budget_pages)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        locks_workspace_init(self.workspace)
+        self.scores = torch.empty(batch, num_kv_heads, max_pages, GROUP, dtype=torch.float32,
+                                  device=device)
+        self.selected = torch.full((batch, num_kv_heads, max(1, budget_pages)), -1,
+                                   dtype=torch.int32, device=device)
+        self.n_selected = torch.zeros(batch, num_kv_heads, dtype=torch.int32, device=device)
+        self.out = torch.empty(batch, num_kv_heads * GROUP, HEAD_DIM, dtype=torch.float32,
+                               device=device)

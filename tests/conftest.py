@@ -24,3 +24,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _library_built():
+    """Build liblocks.so once per session when a GPU is present (GPU tests
+    need it; there is no fallback)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            from sparse_long_context_locks_gb300 import build
+            build.build()
+    except ImportError:
+        pass
+    yield
