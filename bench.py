@@ -1,0 +1,451 @@
+"""Decode-step benchmark of the LOCKS hot path on GB300.
+
+A step is one pass of the decode hot path over one batch of synthetic input:
+page scoring + group-shared top-k selection (locks_score_select) followed by
+sparse paged attention over the selected pages and the open tail page
+(locks_sparse_decode), captured once into a CUDA graph and replayed.  The
+summary builder (run when pages are finalised, off the decode critical path)
+and the dense comparator are timed in the same run and reported under "rows".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload llama8b_128k]
+
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the launching stream; between timed steps L2 is flushed by reading a
+256 MB buffer (the step's inputs are smaller than L2), outside the events.
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling),
+the per-rank times are max-reduced and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-step µs/layer and tokens/s at 128K–1M ctx; achieved HBM GB/s vs peak"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_llama8b_128k.json")
+SCORE_SOURCE = os.path.join(ROOT, "sparse_long_context_locks_gb300", "csrc", "score_select.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="locks", choices=["locks", "reference"])
+    ap.add_argument("--workload", default="llama8b_128k")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[2]), "max": float(parts[3]), "power": float(parts[4]),
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power": parts[9]})
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [r for r in rows if r["power"] > 0] or rows
+        sm = sorted(r["sm"] for r in load)
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r["max"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ------------------------------------------------------------------ oracle baseline
+def _oracle_unit(args):
+    """One (b, h) unit of the decode step in the fp64 oracle (worker process)."""
+    import numpy as np
+    import oracle as O
+    tmp, b, h, G, budget = args
+    rec = np.load(os.path.join(tmp, "rec.npy"), mmap_mode="r")
+    kc = np.load(os.path.join(tmp, "k.npy"), mmap_mode="r")
+    vc = np.load(os.path.join(tmp, "v.npy"), mmap_mode="r")
+    q = np.load(os.path.join(tmp, "q.npy"))
+    bt = np.load(os.path.join(tmp, "bt.npy"))
+    lens = np.load(os.path.join(tmp, "lens.npy"))
+    t0 = time.perf_counter()
+    L_b = int(lens[b])
+    n = L_b // 16
+    qg = q[b, h * G:(h + 1) * G].astype(np.float64)
+    recs = np.asarray(rec[bt[b, :n], h])
+    d = O.dequantize(O.decode_records(recs))
+    s_hat = O.page_scores(qg, d["mu"], d["V"], d["C"])
+    sel, _ = O.select_pages(s_hat, budget)
+    out = O.sparse_attend_unit(qg, kc, vc, bt[b], h, L_b, sel, 1 / math.sqrt(128))
+    return time.perf_counter() - t0, float(np.abs(out).sum())
+
+
+def oracle_host_copy(data, summ, tmp):
+    import numpy as np
+    np.save(os.path.join(tmp, "rec.npy"), summ.cpu().numpy())
+    np.save(os.path.join(tmp, "k.npy"), data["k_cache"].float().cpu().numpy())
+    np.save(os.path.join(tmp, "v.npy"), data["v_cache"].float().cpu().numpy())
+    np.save(os.path.join(tmp, "q.npy"), data["q"].float().cpu().numpy())
+    np.save(os.path.join(tmp, "bt.npy"), data["block_table"].cpu().numpy().astype(np.int64))
+    np.save(os.path.join(tmp, "lens.npy"), data["seq_lens"].cpu().numpy())
+
+
+def run_oracle_sample(tmp, units, G, budget, seconds, pool):
+    """Time the oracle on units (cycled) for about `seconds`; returns per-unit s."""
+    times = []
+    t_start = time.perf_counter()
+    i = 0
+    cores = pool._processes
+    while time.perf_counter() - t_start < seconds or not times:
+        batch = [units[(i + j) % len(units)] for j in range(cores)]
+        i += cores
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_unit, [(tmp, b, h, G, budget) for b, h in batch])
+        wall = time.perf_counter() - t0
+        times.append((wall, len(res)))
+    tot = sum(w for w, _ in times)
+    cnt = sum(c for _, c in times)
+    return tot / cnt, cnt
+
+
+def make_pool():
+    import multiprocessing as mp
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("MKL_NUM_THREADS", "1")
+    ctx = mp.get_context("spawn")
+    return ctx.Pool(cores), cores
+
+
+# ------------------------------------------------------------------ main arm
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+
+    pool = cores = None
+    want_cpu = (args.impl == "reference" or not args.no_cpu_baseline) and rank == 0
+    if want_cpu:
+        pool, cores = make_pool()   # spawned before the first GPU call
+
+    import torch
+    if args.impl == "reference" and rank != 0:
+        return
+    torch.cuda.set_device(local)
+    if world > 1 and args.impl == "locks":
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from sparse_long_context_locks_gb300 import locks as L
+    from sparse_long_context_locks_gb300 import workload as W
+
+    w = W.CONFIGS[args.workload]
+    H, G, B = w.num_kv_heads, w.group, w.batch
+    data = W.generate(w.scaled(seed=w.seed + 7919 * rank), device="cuda")
+    lens = data["seq_lens"].cpu().tolist()
+    by = W.algorithmic_bytes(lens, H, G, w.budget_pages)
+    summ = torch.zeros(data["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
+    blocks = W.full_page_blocks(data).cuda()
+    bufs = L.DecodeBuffers(H, B, w.max_pages, w.budget_pages)
+    L.locks_build_summaries(H, data["k_cache"], blocks, summ, bufs.workspace)
+    torch.cuda.synchronize()
+    config = {"workload": w.name, "batch": B, "context": w.context, "q_heads": H * G,
+              "kv_heads": H, "head_dim": 128, "page": 16, "rank": 8,
+              "budget_tokens": w.budget_tokens, "summary_bytes": 784,
+              "l2": "flushed between timed steps by reading a 256 MB buffer"}
+
+    if args.impl == "reference":
+        tmp = tempfile.mkdtemp(prefix="locks_oracle_")
+        oracle_host_copy(data, summ, tmp)
+        units = [(b, h) for b in range(B) for h in range(H)]
+        for _ in range(max(0, args.warmup)):
+            pool.map(_oracle_unit, [(tmp, *units[0], G, w.budget_pages)])
+        per_unit = []
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            batch = [units[(i * cores + j) % len(units)] for j in range(cores)]
+            ts = time.perf_counter()
+            pool.map(_oracle_unit, [(tmp, b, h, G, w.budget_pages) for b, h in batch])
+            per_unit.append((time.perf_counter() - ts) / len(batch))
+        wall = time.perf_counter() - t0
+        unit_s = sum(per_unit) / len(per_unit)
+        step_s = unit_s * len(units)
+        value = B / step_s
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"each step: {cores} (request, KV head) units of the decode step "
+                                           f"(score from records, select, attend) on {cores} processes; "
+                                           f"time per unit x {len(units)} units"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "wall_s": wall}
+        pool.close()
+        print(json.dumps(line))
+        return
+
+    # ---------------------------------------------------------------- graphs
+    stream = torch.cuda.Stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda").fill_(1.0)
+    sink = torch.zeros(1, device="cuda")
+
+    def step_calls(s):
+        L.locks_score_select(H, data["q"], summ, data["block_table"], data["seq_lens"], w.budget_pages,
+                             bufs.selected, bufs.n_selected, bufs.workspace, scores=bufs.scores, stream=s)
+        L.locks_sparse_decode(H, data["q"], data["k_cache"], data["v_cache"], data["block_table"],
+                              data["seq_lens"], bufs.selected, bufs.n_selected, w.budget_pages, bufs.out,
+                              bufs.workspace, stream=s)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(stream)          # warm (also sets kernel attributes outside capture)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                fn(stream)
+        torch.cuda.synchronize()
+        return g
+
+    g_step = capture(step_calls)
+    g_score = capture(lambda s: L.locks_score(H, data["q"], summ, data["block_table"], data["seq_lens"],
+                                              bufs.workspace, scores=bufs.scores, stream=s))
+    g_select = capture(lambda s: L.locks_select(H, data["seq_lens"], w.max_pages, w.budget_pages,
+                                                bufs.selected, bufs.n_selected, bufs.workspace,
+                                                scores=bufs.scores, stream=s))
+    g_sparse = capture(lambda s: L.locks_sparse_decode(H, data["q"], data["k_cache"], data["v_cache"],
+                                                       data["block_table"], data["seq_lens"], bufs.selected,
+                                                       bufs.n_selected, w.budget_pages, bufs.out,
+                                                       bufs.workspace, stream=s))
+    dense_out = torch.empty_like(bufs.out)
+    g_dense = capture(lambda s: L.locks_dense_decode(H, data["q"], data["k_cache"], data["v_cache"],
+                                                     data["block_table"], data["seq_lens"], dense_out,
+                                                     bufs.workspace, stream=s))
+
+    def flush_l2():
+        torch.sum(flush, out=sink)
+
+    # ---------------------------------------------------------------- timed steps
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush_l2()
+            g_step.replay()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(stream)
+            g_step.replay()
+            ev[i][1].record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clock_rows = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = sum(step_ms) / K
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms_step = float(t.item())
+    value = world * B / (ms_step * 1e-3)
+
+    # ---------------------------------------------------------------- per-kernel rows
+    R = min(200, max(20, K // 10))
+
+    def time_graph(g, reps=R, sleep_cycles=400_000):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                flush_l2()
+                torch.cuda._sleep(sleep_cycles)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+        return tot / reps * 1e3   # us
+
+    us_score = time_graph(g_score)
+    us_select = time_graph(g_select)
+    us_sparse = time_graph(g_sparse)
+    us_dense = time_graph(g_dense, reps=max(10, R // 4))
+    # builder over every full page (prefill-style), timed the same way
+    def build_all(s):
+        L.locks_build_summaries(H, data["k_cache"], blocks, summ, bufs.workspace, stream=s)
+    g_build = capture(build_all)
+    us_build = time_graph(g_build, reps=max(5, R // 10))
+    n_page_heads = int(blocks.numel()) * H
+
+    peak, peak_src = peaks()
+    score_gbs = by["score"] / (us_score * 1e-6) / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            prof = json.load(f)
+        src_hash = hashlib.sha256(open(SCORE_SOURCE, "rb").read()).hexdigest()[:16]
+        if prof.get("source_sha256_16") == src_hash and prof.get("workload") == w.name:
+            traffic = prof.get("dram_bytes_per_launch")
+    except Exception:
+        traffic = None
+
+    # ---------------------------------------------------------------- e2e
+    q_host = data["q"].cpu().pin_memory()
+    lens_host = data["seq_lens"].cpu().pin_memory()
+    out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    E = min(K, 500)
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            data["q"].copy_(q_host, non_blocking=True)
+            g_step.replay()
+            out_host.copy_(bufs.out, non_blocking=True)
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(E):
+            data["q"].copy_(q_host, non_blocking=True)
+            data["seq_lens"].copy_(lens_host, non_blocking=True)
+            g_step.replay()
+            out_host.copy_(bufs.out, non_blocking=True)
+            stream.synchronize()
+        e2e_s = (time.perf_counter() - t0) / E
+    h2d = q_host.numel() * q_host.element_size() + lens_host.numel() * 4
+    d2h = out_host.numel() * out_host.element_size()
+
+    status = L.locks_read_status(bufs.workspace)
+
+    # ---------------------------------------------------------------- cpu baseline
+    cpu = None
+    if want_cpu and pool is not None:
+        tmp = tempfile.mkdtemp(prefix="locks_oracle_")
+        oracle_host_copy(data, summ, tmp)
+        units = [(b, h) for b in range(B) for h in range(H)]
+        unit_s, cnt = run_oracle_sample(tmp, units, G, w.budget_pages, args.cpu_seconds, pool)
+        cpu_step = unit_s * len(units)
+        cpu = {"value": B / cpu_step, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{cnt} (request, KV head) units of this workload's decode step (score from "
+                         f"the GPU-built records, select, attend) on {cores} spawned processes, "
+                         f"scaled to the {len(units)} units of one step",
+               "ms_per_step": cpu_step * 1e3}
+        pool.close()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config,
+        "clocks": ClockSampler.summary(clock_rows),
+        "e2e": {"value": w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "mode": "pinned H2D of q and seq_lens, graph replay of the two C-ABI calls, "
+                        "D2H of out, host wall clock incl. stream sync"},
+        "gpu_launches": 3 * K,
+        "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": score_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": by["score"], "peak_source": peak_src},
+        "rows": {
+            "score_us": us_score, "select_us": us_select, "sparse_attention_us": us_sparse,
+            "step_us": ms_step * 1e3,
+            "step_GBps": by["step"] / (ms_step * 1e-3) / 1e9,
+            "sparse_attention_GBps": by["sparse_kv"] / (us_sparse * 1e-6) / 1e9,
+            "dense_us": us_dense, "dense_GBps": by["dense_kv"] / (us_dense * 1e-6) / 1e9,
+            "dense_frac": by["dense_kv"] / (us_dense * 1e-6) / 1e9 / peak,
+            "build_us": us_build, "build_page_heads": n_page_heads,
+            "build_GBps": (n_page_heads * (4096 + 784)) / (us_build * 1e-6) / 1e9,
+            "bytes_step": by["step"], "bytes_dense": by["dense_step"],
+            "bytes_ratio_dense_over_step": by["dense_step"] / by["step"],
+            "latency_ratio_dense_over_step": us_dense / (ms_step * 1e3),
+        },
+        "cpu_baseline": cpu,
+        "status_flags": status,
+        "wall_timed_s": t_wall,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -72,17 +72,19 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   pl.dense_ips = ceil_div(max_pages, pl.dense_splits);
   pl.max_splits = max(pl.sparse_splits, pl.dense_splits);
 
+  // Regions whose size or position does not depend on the budget come first,
+  // so every call of a step (whatever budget it passes) agrees on them.
   size_t off = kAlign;  // [0, 256): status word
+  pl.off_tickets = off;
+  off = align_up(off + (size_t)units * sizeof(uint32_t));
   pl.off_partials = off;
   off = align_up(off + (size_t)batch * H * pl.n_chunks * pl.wph * kGroup * 2 * sizeof(float));
   pl.off_scores = off;
   off = align_up(off + (size_t)batch * H * max_pages * kGroup * sizeof(float));
   pl.off_keys = off;
   off = align_up(off + (size_t)batch * H * max_pages * sizeof(uint32_t));
-  pl.off_attn = off;
+  pl.off_attn = off;   // last: its size depends on the split counts
   off = align_up(off + (size_t)units * pl.max_splits * kGroup * (2 + kHeadDim) * sizeof(float));
-  pl.off_tickets = off;
-  off = align_up(off + (size_t)units * sizeof(uint32_t));
   pl.total = off;
   return pl;
 }

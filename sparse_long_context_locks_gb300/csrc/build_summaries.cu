@@ -14,8 +14,7 @@
 //   2. lane i computes row i of the Gram matrix G = X X^T (16 x 16, fp32);
 //   3. parallel cyclic Jacobi (round-robin pairing, 8 disjoint rotations per
 //      round, 15 rounds per sweep) with lane i owning row i of G and of the
-//      eigenvector matrix W; sweeps stop when the off-diagonal mass is below
-//      1e-12 of the total (at most kMaxSweeps);
+//      eigenvector matrix W; kSweeps sweeps;
 //   4. eigenvalues ranked (descending, lower index on ties), top 8 kept,
 //      sign fixed so the largest |coefficient| of each direction is positive,
 //      lambda_k <= 1e-6 lambda_1 -> zero direction;
@@ -33,7 +32,7 @@ namespace locks {
 constexpr int kBuildWarps = 4;
 constexpr int kBuildThreads = kBuildWarps * 32;
 constexpr int kXStride = 132;          // padded fp32 row of X (conflict-free LDS.128)
-constexpr int kMaxSweeps = 12;
+constexpr int kSweeps = 8;
 
 struct HalfWarpSmem {
   float X[kPage * kXStride];           // centred keys
@@ -194,22 +193,11 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     *reinterpret_cast<float4*>(&S.G[i * kPage + j]) = make_float4(g[j], g[j + 1], g[j + 2], g[j + 3]);
   __syncwarp();
 
-  // ---- 3. Jacobi sweeps
-  for (int sweep = 0; sweep < kMaxSweeps; ++sweep) {
-    float tot = 0.f;
-#pragma unroll
-    for (int j = 0; j < kPage; ++j) tot = fmaf(g[j], g[j], tot);
-    const float dii = S.G[i * kPage + i];
-    float off = tot - dii * dii;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      off += __shfl_xor_sync(0xffffffffu, off, o);
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    }
-    const bool done = !(off > 1e-12f * tot);
-    if (__all_sync(0xffffffffu, done)) break;
-    Sweep<0>::run(g, w, i, hbase, S);
-  }
+  // ---- 3. Jacobi sweeps.  A fixed count: stopping on the off-diagonal mass
+  // relative to the whole matrix (dominated by lambda_1) leaves pairs of small
+  // eigenvalues coupled; in fp32 the top-8 directions reach their rounding
+  // floor after 7 sweeps on low-rank, noisy and full-rank pages alike.
+  for (int sweep = 0; sweep < kSweeps; ++sweep) Sweep<0>::run(g, w, i, hbase, S);
 
   // ---- 4. rank eigenvalues, pick the top r, fix signs
 #pragma unroll

@@ -172,10 +172,11 @@ def check_records(gpu_rec: np.ndarray, K_pages: np.ndarray) -> dict:
     scale = np.maximum(lam[:, :1], 1e-30)
     gaps = -np.diff(lam[:, :9], axis=1) / scale           # gaps among the top 9
     well = np.all(gaps > 1e-3, axis=1) & (lam[:, 7] > 1e-3 * lam[:, 0])
-    # scales
-    for key in ("sV", "smu", "sC"):
-        ref = qo[key]
-        np.testing.assert_allclose(g[key], ref, rtol=2e-4, atol=1e-30, err_msg=key)
+    # scales: the centroid's always, the basis/coefficient ones where the top-9
+    # spectrum is well separated (elsewhere individual directions are not unique)
+    np.testing.assert_allclose(g["smu"], qo["smu"], rtol=2e-6, atol=1e-30, err_msg="smu")
+    for key in ("sV", "sC"):
+        np.testing.assert_allclose(g[key][well], qo[key][well], rtol=2e-4, atol=1e-30, err_msg=key)
     np.testing.assert_allclose(g["tail"], summ["tail"], rtol=2e-3, atol=1e-4 * float(lam[:, 0].max()))
 
     def code_ok(gc, oc_val, s):
