@@ -260,7 +260,7 @@ def main():
     # ---------------------------------------------------------------- graphs
     stream = torch.cuda.Stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda").fill_(1.0)
-    sink = torch.zeros(1, device="cuda")
+    sink = torch.zeros((), device="cuda")
 
     def step_calls(s):
         L.locks_score_select(H, data["q"], summ, data["block_table"], data["seq_lens"], w.budget_pages,
@@ -295,7 +295,7 @@ def main():
                                                      bufs.workspace, stream=s))
 
     def flush_l2():
-        torch.sum(flush, out=sink)
+        torch.sum(flush, dim=0, out=sink)
 
     # ---------------------------------------------------------------- timed steps
     with torch.cuda.stream(stream):

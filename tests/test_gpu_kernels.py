@@ -34,7 +34,7 @@ def test_build_summaries_parity(noise):
     n = run.lens[0] // 16
     K = run.pages_f64(run.d["k_cache"], 0, 0, range(n))
     info = check_records(run.records(0, 0), K)
-    assert info["well_conditioned"] > 0.9 * n
+    assert info["well_conditioned"] > 0.75 * n
 
 
 def test_build_summaries_fullrank_and_multihead():
