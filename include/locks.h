@@ -194,6 +194,26 @@ locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void 
                                 int32_t batch, int32_t max_pages, float sm_scale, float *out,
                                 void *workspace, size_t workspace_bytes, locks_stream_t stream);
 
+/* Sparse decode attention without a caller-provided workspace.  The paper
+ * has no counterpart: this exists for callers that cannot allocate device
+ * memory (an engine that gave all of HBM to its KV-cache pool, a
+ * latency-critical path where cudaMalloc would synchronise the device, a host
+ * integration with no allocator).  Same computation, arguments and layouts as
+ * locks_sparse_decode; the scratch (split partials, merge tickets, status
+ * word) is one fixed 8 MiB device array inside the library, resident on every
+ * GPU that loads it until exit.  Allocates nothing.  The first call on a
+ * device looks up that array's address (make it before any stream capture);
+ * each call clears the tickets and status with one cudaMemsetAsync on
+ * `stream`.  Calls share the array: calls that overlap on the GPU race.
+ * Returns LOCKS_ERR_WORKSPACE when batch * H_kv * splits partial states do
+ * not fit in 8 MiB (e.g. beyond ~4000 request-head-split slots). */
+locks_status locks_sparse_decode_noalloc(const locks_cfg *cfg, const void *q, const void *k_cache,
+                                         const void *v_cache, int64_t num_blocks,
+                                         const int32_t *block_table, const int32_t *seq_lens,
+                                         const int32_t *selected, const int32_t *n_selected,
+                                         int32_t batch, int32_t max_pages, int32_t budget_pages,
+                                         float sm_scale, float *out, locks_stream_t stream);
+
 /* Static description of a status code. */
 const char *locks_status_str(locks_status status);
 

@@ -59,6 +59,8 @@ _SIGS = {
     "locks_dense_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _I32, _F, _P, _P, _SZ,
                                   _P]),
     "locks_status_str": (ctypes.c_char_p, [_I32]),
+    "locks_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32,
+                                           _I32, _F, _P, _P]),
 }
 
 
@@ -189,6 +191,19 @@ def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens,
         ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
         _ptr(block_table), _ptr(seq_lens), block_table.shape[0], block_table.shape[1], scale,
         _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_dense_decode")
+
+
+def locks_sparse_decode_noalloc(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, selected,
+                                n_selected, budget_pages, out, sm_scale=None, stream=None):
+    """locks_sparse_decode for callers that cannot allocate: the library's own
+    fixed device scratch replaces the workspace (see include/locks.h)."""
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_sparse_decode_noalloc(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_table), _ptr(seq_lens), _ptr(selected), _ptr(n_selected),
+        block_table.shape[0], block_table.shape[1], budget_pages, scale, _ptr(out),
+        _stream(stream)), "locks_sparse_decode_noalloc")
 
 
 def locks_status_str(status: int) -> str:
