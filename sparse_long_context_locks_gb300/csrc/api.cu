@@ -27,11 +27,12 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   // scoring
-  int h_cta, wph, pps, head_groups, ch_pages, n_chunks, n_items, score_grid;
+  int h_cta, wph, pps, head_groups, ch_pages, n_chunks, n_items, score_grid, seg_slots;
+  // selection
   // attention
   int sparse_splits, sparse_ips, dense_splits, dense_ips, max_splits;
   // workspace regions
-  size_t off_partials, off_scores, off_keys, off_attn, off_tickets, total;
+  size_t off_partials, off_scores, off_attn, off_tickets, total;
 };
 
 bool cfg_supported(const locks_cfg* c) {
@@ -60,11 +61,14 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   pl.wph = 8 / pl.h_cta;
   pl.pps = 4 * pl.wph;
   pl.head_groups = H / pl.h_cta;
-  pl.ch_pages = 8 * pl.pps;
+  pl.ch_pages = pl.pps;   // one stage per work item: the grid splits evenly
   pl.n_chunks = ceil_div(max_pages, pl.ch_pages);
   const int64_t items = (int64_t)batch * pl.head_groups * pl.n_chunks;
   pl.n_items = (int)items;
   pl.score_grid = (int)(items < kTargetCtas ? items : kTargetCtas);
+  // a CTA's contiguous item range touches at most this many units
+  const int64_t per_cta = (items + pl.score_grid - 1) / pl.score_grid;
+  pl.seg_slots = (int)((per_cta + pl.n_chunks - 1) / pl.n_chunks + 1);
   const int units = batch * H;
   pl.sparse_splits = pick_splits(units, budget + 1);
   pl.sparse_ips = ceil_div(budget + 1, pl.sparse_splits);
@@ -78,11 +82,9 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   pl.off_tickets = off;
   off = align_up(off + (size_t)units * sizeof(uint32_t));
   pl.off_partials = off;
-  off = align_up(off + (size_t)batch * H * pl.n_chunks * pl.wph * kGroup * 2 * sizeof(float));
+  off = align_up(off + (size_t)pl.score_grid * pl.seg_slots * 8 * kGroup * 2 * sizeof(float));
   pl.off_scores = off;
   off = align_up(off + (size_t)batch * H * max_pages * kGroup * sizeof(float));
-  pl.off_keys = off;
-  off = align_up(off + (size_t)batch * H * max_pages * sizeof(uint32_t));
   pl.off_attn = off;   // last: its size depends on the split counts
   off = align_up(off + (size_t)units * pl.max_splits * kGroup * (2 + kHeadDim) * sizeof(float));
   pl.total = off;
@@ -278,6 +280,7 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   p.n_chunks = pl.n_chunks;
   p.head_groups = pl.head_groups;
   p.n_items = pl.n_items;
+  p.seg_slots = pl.seg_slots;
   return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -293,6 +296,7 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   LOCKS_CHECK_PTR(workspace);
   if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
   if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  if ((max_pages + kSelCluster - 1) / kSelCluster > kSelMaxKeysPerCta) return LOCKS_ERR_UNSUPPORTED;
   const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
   if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -300,7 +304,6 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   p.seq_lens = seq_lens;
   p.scores = scores ? scores : reinterpret_cast<const float*>(ws + pl.off_scores);
   p.partials = reinterpret_cast<const float*>(ws + pl.off_partials);
-  p.keys = reinterpret_cast<uint32_t*>(ws + pl.off_keys);
   p.selected = selected;
   p.n_selected = n_selected;
   p.status = status_word(workspace);
@@ -308,7 +311,12 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   p.max_pages = max_pages;
   p.H_kv = cfg->num_kv_heads;
   p.budget = budget_pages;
+  p.score_grid = pl.score_grid;
+  p.seg_slots = pl.seg_slots;
+  p.n_items = pl.n_items;
   p.n_chunks = pl.n_chunks;
+  p.head_groups = pl.head_groups;
+  p.h_cta = pl.h_cta;
   p.wph = pl.wph;
   return from_cuda(launch_select(p, batch * cfg->num_kv_heads, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -23,6 +23,8 @@ constexpr int kRank = 8;
 constexpr int kGroup = 4;
 constexpr int kRecord = 784;
 constexpr int kTargetCtas = 304;   // 2 resident CTAs x 152 SMs (GB300)
+constexpr int kSelCluster = 8;     // CTAs per (request, KV head) in the selection
+constexpr int kSelMaxKeysPerCta = 50000;   // 200 KB of keys in shared memory
 
 // ---------------------------------------------------------------- status
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bit) {
@@ -195,6 +197,26 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
   lo = h2_sub(a, 0x64806480u);                               // - 1152
   hi = h2_sub(b, 0x64806480u);
+}
+
+// Biased variants for tensor-core operands whose offset is removed once, in
+// the accumulator's starting value, instead of per element.
+// Eight int4 codes -> four f16x2 pairs of (72 + code), exact: each nibble is
+// moved to bits 4-7 of a half and or-ed under the exponent of 64 (0x5400),
+// where those bits are worth 1 (nibble n ^ 8 = code + 8).
+__device__ __forceinline__ void nib8_to_h2x4_b72(uint32_t w, uint32_t& p04, uint32_t& p15,
+                                                 uint32_t& p26, uint32_t& p37) {
+  p04 = and_xor(w << 4, 0x00F000F0u, 0x54805480u);
+  p15 = and_xor(w, 0x00F000F0u, 0x54805480u);
+  p26 = and_xor(w >> 4, 0x00F000F0u, 0x54805480u);
+  p37 = and_xor(w >> 8, 0x00F000F0u, 0x54805480u);
+}
+
+// Four int8 codes [b0 b1 b2 b3] -> f16x2 (1152 + b0, 1152 + b1), (1152 + b2, 1152 + b3).
+__device__ __forceinline__ void i8x4_to_h2x2_b1152(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  lo = __byte_perm(x, 0x64646464u, 0x4140);
+  hi = __byte_perm(x, 0x64646464u, 0x4342);
 }
 
 // fp32 pair -> f16x2 high part and f16x2 residual (x ~= hi + lo to ~2^-22).

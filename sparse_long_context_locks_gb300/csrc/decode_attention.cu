@@ -338,23 +338,70 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
-  // last CTA of the unit: combine all splits
+  // last CTA of the unit: combine all splits.  Max and weights are computed
+  // cooperatively (split sp -> thread sp mod 128), then every thread (one
+  // output dim) sums the splits' partial outputs with many loads in flight.
   const float* up = p.part + (int64_t)unit * p.splits * kGroup * kPartStride;
+  const int S = p.splits;
+  float* red = reinterpret_cast<float*>(smem + 12288);   // [warp][G] reductions
+  float* wsm = reinterpret_cast<float*>(smem + 16384);   // [S][G] split weights
+  float mloc[kGroup], lloc[kGroup];
 #pragma unroll
   for (int g = 0; g < kGroup; ++g) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(up + (sp * kGroup + g) * kPartStride));
-    float Ls = 0.f, Os = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < p.splits; ++sp) {
-        const float* q = up + (sp * kGroup + g) * kPartStride;
-        const float f = fast_exp2(__ldcg(q) - M);
-        Ls += __ldcg(q + 1) * f;
-        Os += __ldcg(q + 2 + d) * f;
-      }
-    }
-    orow[g * kHeadDim + d] = Ls > 0.f ? Os / Ls : 0.f;
+    mloc[g] = -INFINITY;
+    lloc[g] = 0.f;
   }
+  for (int sp = threadIdx.x; sp < S; sp += blockDim.x)
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) mloc[g] = fmaxf(mloc[g], __ldcg(up + (sp * kGroup + g) * kPartStride));
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc[g] = fmaxf(mloc[g], __shfl_xor_sync(0xffffffffu, mloc[g], o));
+    if (lane == 0) red[warp * kGroup + g] = mloc[g];
+  }
+  __syncthreads();
+  float Mall[kGroup];
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    Mall[g] = red[g];
+    for (int w = 1; w < kAttnWarps; ++w) Mall[g] = fmaxf(Mall[g], red[w * kGroup + g]);
+  }
+  __syncthreads();
+  for (int sp = threadIdx.x; sp < S; sp += blockDim.x) {
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const float* q = up + (sp * kGroup + g) * kPartStride;
+      const float f = Mall[g] == -INFINITY ? 0.f : fast_exp2(__ldcg(q) - Mall[g]);
+      wsm[sp * kGroup + g] = f;
+      lloc[g] += __ldcg(q + 1) * f;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lloc[g] += __shfl_xor_sync(0xffffffffu, lloc[g], o);
+    if (lane == 0) red[warp * kGroup + g] = lloc[g];
+  }
+  __syncthreads();
+  float Lall[kGroup], acc_o[kGroup];
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    Lall[g] = 0.f;
+    for (int w = 0; w < kAttnWarps; ++w) Lall[g] += red[w * kGroup + g];
+    acc_o[g] = 0.f;
+  }
+#pragma unroll 4
+  for (int sp = 0; sp < S; ++sp) {
+    const float4 wv = *reinterpret_cast<const float4*>(wsm + sp * kGroup);
+    const float* q = up + sp * kGroup * kPartStride + 2 + d;
+    acc_o[0] += wv.x * __ldcg(q);
+    acc_o[1] += wv.y * __ldcg(q + kPartStride);
+    acc_o[2] += wv.z * __ldcg(q + 2 * kPartStride);
+    acc_o[3] += wv.w * __ldcg(q + 3 * kPartStride);
+  }
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) orow[g * kHeadDim + d] = Lall[g] > 0.f ? acc_o[g] / Lall[g] : 0.f;
   if (threadIdx.x == 0) p.tickets[unit] = 0;   // ready for the next call
 }
 

@@ -27,6 +27,9 @@
 #include "common.cuh"
 #include "params.h"
 
+#include <cooperative_groups.h>
+namespace cg = cooperative_groups;
+
 namespace locks {
 
 
@@ -49,8 +52,12 @@ __device__ __forceinline__ int request_full_pages(const ScoreParams& p, int b) {
 // Returns s for the lane's two rows: row gid = (page gid>>2, head gid&3) and
 // row gid+8 = (page 2 + (gid>>2), head gid&3); identical on the 4 lanes of a
 // row quad.
+// bias_v / bias_mu: the constant parts the biased code conversions add to
+// V^T q and q . mu for this lane's columns 2t and 2t+1 (removed by starting
+// the accumulators at -bias).
 __device__ __forceinline__ void score_group4(const uint8_t* rec0, int stride,
                                              const uint32_t (&qb)[8][2], float pow2e,
+                                             const float (&bias_v)[2], const float (&bias_mu)[2],
                                              int lane, float& s_r0, float& s_r1) {
   const int gid = lane >> 2, t = lane & 3;
   const float inv_sqrt_d = 0.08838834764831845f;
@@ -63,24 +70,27 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, int stride,
   float d1[2][4];
 #pragma unroll
   for (int pr = 0; pr < 2; ++pr) {
+    float e1[4] = {0.f, 0.f, 0.f, 0.f};   // second chain: odd k-steps
     const uint4 va = *reinterpret_cast<const uint4*>(rec0 + (2 * pr) * stride + gid * 64 + t * 16);
     const uint4 vb = *reinterpret_cast<const uint4*>(rec0 + (2 * pr + 1) * stride + gid * 64 + t * 16);
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d1[pr][i] = 0.f;
+    d1[pr][0] = d1[pr][2] = -bias_v[0];
+    d1[pr][1] = d1[pr][3] = -bias_v[1];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-      nib8_to_h2x4(wa[w], a04, a15, a26, a37);
-      nib8_to_h2x4(wb[w], b04, b15, b26, b37);
+      nib8_to_h2x4_b72(wa[w], a04, a15, a26, a37);
+      nib8_to_h2x4_b72(wb[w], b04, b15, b26, b37);
       mma_f16(d1[pr], a04, b04, a15, b15, qb[2 * w][0], qb[2 * w][1]);
-      mma_f16(d1[pr], a26, b26, a37, b37, qb[2 * w + 1][0], qb[2 * w + 1][1]);
+      mma_f16(e1, a26, b26, a37, b37, qb[2 * w + 1][0], qb[2 * w + 1][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d1[pr][i] += e1[i];
   }
 
   // ---- q . mu for the 4 pages (rows 0..3 of one m16 tile)
-  float dmu[4] = {0.f, 0.f, 0.f, 0.f};
+  float dmu[4] = {-bias_mu[0], -bias_mu[1], -bias_mu[0], -bias_mu[1]};
   {
     uint4 m0 = make_uint4(0, 0, 0, 0), m1 = make_uint4(0, 0, 0, 0);
     if (gid < 4) {
@@ -92,7 +102,7 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, int stride,
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       uint32_t lo = 0, hi = 0;
-      if (gid < 4) i8x4_to_h2x2(mw[s], lo, hi);
+      if (gid < 4) i8x4_to_h2x2_b1152(mw[s], lo, hi);
       mma_f16(dmu, lo, 0u, hi, 0u, qb[s][0], qb[s][1]);
     }
   }
@@ -176,12 +186,9 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, int stride,
 }
 
 __device__ __forceinline__ void lse_push(float& m, float& s, float x) {
-  if (x > m) {
-    s = s * fast_exp2((m - x) * kLog2e) + 1.f;
-    m = x;
-  } else {
-    s += fast_exp2((x - m) * kLog2e);
-  }
+  const float mn = fmaxf(m, x);
+  s = s * fast_exp2((m - mn) * kLog2e) + fast_exp2((x - mn) * kLog2e);
+  m = mn;
 }
 
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
@@ -216,45 +223,73 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
   }
   __syncthreads();
 
+  // This CTA's contiguous range of work items (one stage = pps pages of one
+  // (request, head group) unit each), split evenly over the grid.
   const int it_begin = (int)(((long long)blockIdx.x * p.n_items) / gridDim.x);
   const int it_end = (int)(((long long)(blockIdx.x + 1) * p.n_items) / gridDim.x);
   const int per_head_rec = p.h_cta * kRecord;
+  const int first_unit = it_begin / p.n_chunks;
 
   if (warp == kScoreConsumers) {
     // ------------------------------------------------------------ producer
+    // Walks the same stage sequence as the consumers; the block ids of the
+    // next stage are loaded while the current stage's copies are issued.
     uint32_t step = 0;
     bool ok = true;
-    for (int item = it_begin; item < it_end && ok; ++item) {
-      const int unit = item / p.n_chunks, c = item % p.n_chunks;
-      const int b = unit / p.head_groups, hg = unit % p.head_groups;
-      const int n = request_full_pages(p, b);
-      const int page0 = c * p.ch_pages;
-      const int page1 = min(page0 + p.ch_pages, max(n, 0));
-      for (int pg = page0; pg < page1 && ok; pg += p.pps, ++step) {
-        const int s = step % kScoreStages;
-        if (step >= kScoreStages) ok = mbar_wait(&empty[s], ((step / kScoreStages) - 1) & 1, p.status);
-        if (!ok) break;
-        const int j = pg + lane;
-        bool is_live = lane < p.pps && j < page1;
-        int64_t blk = -1;
-        if (is_live) {
-          blk = p.block_table[(int64_t)b * p.max_pages + j];
-          if (blk < 0 || blk >= p.num_blocks) {
-            flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
-            is_live = false;
-          }
-        }
-        const uint32_t mask = __ballot_sync(0xffffffffu, is_live);
-        if (lane == 0) {
-          live[s] = mask;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(mask) * (uint32_t)per_head_rec);
-        }
-        __syncwarp();
-        if (is_live) {
-          const uint8_t* src = p.summ + ((int64_t)blk * p.H_kv + (int64_t)hg * p.h_cta) * kRecord;
-          bulk_g2s(stages + s * kScoreStageBytes + lane * per_head_rec, src, per_head_rec, &full[s]);
-        }
+    int unit = first_unit, c = it_begin - first_unit * p.n_chunks;
+    int it = it_begin;
+    int b = 0, hg = 0, n = 0;
+    auto enter_unit = [&]() {
+      b = unit / p.head_groups;
+      hg = unit % p.head_groups;
+      n = max(request_full_pages(p, b), 0);
+    };
+    // advance (it, c, unit) to the next stage that holds pages, or it_end
+    auto skip_empty = [&]() {
+      while (it < it_end && c * p.pps >= n) {
+        const int unit_end = (unit + 1) * p.n_chunks;
+        it = unit_end;
+        c = 0;
+        ++unit;
+        if (it < it_end) enter_unit();
       }
+    };
+    if (it < it_end) enter_unit();
+    skip_empty();
+    int64_t blk = -1;
+    if (it < it_end && lane < p.pps && c * p.pps + lane < n)
+      blk = p.block_table[(int64_t)b * p.max_pages + c * p.pps + lane];
+    while (it < it_end && ok) {
+      const int s = step % kScoreStages;
+      if (step >= kScoreStages) ok = mbar_wait(&empty[s], ((step / kScoreStages) - 1) & 1, p.status);
+      if (!ok) break;
+      bool is_live = lane < p.pps && c * p.pps + lane < n;
+      if (is_live && (blk < 0 || blk >= p.num_blocks)) {
+        flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+        is_live = false;
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, is_live);
+      if (lane == 0) {
+        live[s] = mask;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(mask) * (uint32_t)per_head_rec);
+      }
+      __syncwarp();
+      if (is_live) {
+        const uint8_t* src = p.summ + ((int64_t)blk * p.H_kv + (int64_t)hg * p.h_cta) * kRecord;
+        bulk_g2s(stages + s * kScoreStageBytes + lane * per_head_rec, src, per_head_rec, &full[s]);
+      }
+      ++step;
+      ++it;
+      ++c;
+      if (c == p.n_chunks) {
+        c = 0;
+        ++unit;
+        if (it < it_end) enter_unit();
+      }
+      skip_empty();
+      blk = -1;
+      if (it < it_end && lane < p.pps && c * p.pps + lane < n)
+        blk = p.block_table[(int64_t)b * p.max_pages + c * p.pps + lane];
     }
     return;
   }
@@ -266,18 +301,23 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
   int cur_b = -1, cur_h = -1;
   uint32_t qb[8][2];
   float pow2e = 1.f;
+  float bias_v[2] = {0.f, 0.f}, bias_mu[2] = {0.f, 0.f};
   bool ok = true;
 
-  for (int item = it_begin; item < it_end; ++item) {
-    const int unit = item / p.n_chunks, c = item % p.n_chunks;
+  int it = it_begin;
+  for (int unit = first_unit; it < it_end; ++unit) {
+    // one segment: this unit's items inside the range
+    const int unit_end = min(it_end, (unit + 1) * p.n_chunks);
     const int b = unit / p.head_groups, hg = unit % p.head_groups;
     const int h = hg * p.h_cta + hl;
-    const int n = request_full_pages(p, b);
-    if (n < 0 && lane == 0 && warp == 0 && c == 0 && hg == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
-    const int page0 = c * p.ch_pages;
-    const int page1 = min(page0 + p.ch_pages, max(n, 0));
+    const int nraw = request_full_pages(p, b);
+    if (nraw < 0 && lane == 0 && warp == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
+    const int n = max(nraw, 0);
+    const int c0 = it - unit * p.n_chunks;
+    const int pg_begin = c0 * p.pps;
+    const int pg_end = min((unit_end - unit * p.n_chunks) * p.pps, n);
 
-    if (page0 < page1 && (b != cur_b || h != cur_h)) {
+    if (pg_begin < pg_end && (b != cur_b || h != cur_h)) {
       // B operand = the group's 4 query heads (duplicated into columns 4..7),
       // pre-scaled by an exact power of two so every value fits f16.
       cur_b = b;
@@ -303,28 +343,41 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
       const int e = ex > 15 ? ex - 15 : 0;
       pow2e = ldexpf(1.f, e);
       const float inv = ldexpf(1.f, -e);
+      float qsum = 0.f;   // sum of this lane's f16 operand values of column gid
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const __half2 lo = __floats2half2_rn(qv[s][0] * inv, qv[s][1] * inv);
         const __half2 hi = __floats2half2_rn(qv[s][2] * inv, qv[s][3] * inv);
         qb[s][0] = *reinterpret_cast<const uint32_t*>(&lo);
         qb[s][1] = *reinterpret_cast<const uint32_t*>(&hi);
+        const float2 lf = __half22float2(lo), hf = __half22float2(hi);
+        qsum += (lf.x + lf.y) + (hf.x + hf.y);
       }
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);   // column gid's sum over all 128 dims
+      // this lane's accumulator columns are 2t and 2t+1: their sums live on
+      // the lanes with gid == 2t and gid == 2t+1
+      const float q0 = __shfl_sync(0xffffffffu, qsum, (2 * t) * 4);
+      const float q1 = __shfl_sync(0xffffffffu, qsum, (2 * t + 1) * 4);
+      bias_v[0] = 72.f * q0;
+      bias_v[1] = 72.f * q1;
+      bias_mu[0] = 1152.f * q0;
+      bias_mu[1] = 1152.f * q1;
     }
 
     float run_m = -INFINITY, run_s = 0.f;   // this lane's head (gid & 3), t == 0 lanes count
-    for (int pg = page0; pg < page1; pg += p.pps, ++step) {
+    float* srow = p.scores + (((int64_t)b * p.H_kv + h) * p.max_pages) * kGroup + (gid & 3);
+    for (int pg = pg_begin; pg < pg_end; pg += p.pps, ++step) {
       const int s = step % kScoreStages;
       if (ok) ok = mbar_wait(&full[s], (step / kScoreStages) & 1, p.status);
       if (ok) {
         const uint32_t mask = live[s];
         const uint8_t* rec0 = stages + s * kScoreStageBytes + (sub * 4) * per_head_rec + hl * kRecord;
         float s_r0, s_r1;
-        score_group4(rec0, per_head_rec, qb, pow2e, lane, s_r0, s_r1);
+        score_group4(rec0, per_head_rec, qb, pow2e, bias_v, bias_mu, lane, s_r0, s_r1);
         const int slot0 = sub * 4 + (gid >> 2), slot1 = sub * 4 + 2 + (gid >> 2);
         const bool v0 = (mask >> slot0) & 1u, v1 = (mask >> slot1) & 1u;
         if (t == 0) {
-          float* srow = p.scores + (((int64_t)b * p.H_kv + h) * p.max_pages) * kGroup + (gid & 3);
           if (v0) {
             srow[(int64_t)(pg + slot0) * kGroup] = s_r0;
             lse_push(run_m, run_s, s_r0);
@@ -338,15 +391,17 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    it = unit_end;
 
-    // partial log-sum-exp of this warp's pages, per query head g = gid & 3:
-    // rows gid and gid ^ 4 hold the same head -> lanes l and l ^ 16.
+    // partial log-sum-exp of this warp's pages of the segment, per query head
+    // g = gid & 3: rows gid and gid ^ 4 hold the same head -> lanes l, l ^ 16.
     const float om = __shfl_xor_sync(0xffffffffu, run_m, 16);
     const float os = __shfl_xor_sync(0xffffffffu, run_s, 16);
     lse_merge(run_m, run_s, om, os);
     if (t == 0 && gid < 4) {
+      const int seg = unit - first_unit;
       float* part = p.partials +
-                    (((((int64_t)b * p.H_kv + h) * p.n_chunks + c) * p.wph + sub) * kGroup + gid) * 2;
+                    ((((int64_t)blockIdx.x * p.seg_slots + seg) * kScoreConsumers + warp) * kGroup + gid) * 2;
       part[0] = run_m;
       part[1] = run_s;
     }
@@ -356,10 +411,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // ---------------------------------------------------------------- select
 
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 256;
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
   int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -369,7 +425,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& t
   if (lane == 31) warp_buf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? warp_buf[lane] : 0;
+    int w = lane < nw ? warp_buf[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
@@ -378,27 +434,55 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& t
     warp_buf[lane] = w;   // inclusive over warps
   }
   __syncthreads();
-  total = warp_buf[(blockDim.x >> 5) - 1];
+  total = warp_buf[nw - 1];
   const int before = (warp > 0 ? warp_buf[warp - 1] : 0) + x - v;
   __syncthreads();
   return before;
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
-  __shared__ float red_m[32][kGroup], red_s[32][kGroup];
-  __shared__ float zg[kGroup];
-  __shared__ int hist[256];
+// Warp-aggregated shared-memory histogram add: lanes holding the same bin add once.
+__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(0xffffffffu, active);
+  if (active) {
+    const uint32_t peers = __match_any_sync(act, bin);
+    if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (int)__popc(peers));
+  }
+}
+
+// First item of CTA c of the scoring grid.
+__device__ __forceinline__ long long score_item_begin(const SelectParams& p, int c) {
+  return ((long long)c * p.n_items) / p.score_grid;
+}
+
+// One cluster of kSelCluster CTAs per (request, KV head).  CTA r keeps the
+// keys of pages [n r / C, n (r+1) / C) in its shared memory.  A radix select
+// (four 8-bit digits, MSB first) finds the kk-th largest key: each pass every
+// CTA histograms its own keys, one cluster barrier, then every CTA sums the C
+// histograms through distributed shared memory and takes the same digit
+// decision.  Compaction: per-CTA counts exchanged the same way give each CTA
+// its output offset, so indices come out in ascending page order.
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+    select_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) uint32_t keys_s[];   // this CTA's slice of keys
+  __shared__ int hist[2][256];
+  __shared__ int tot[256];
+  __shared__ int slice_cnt[2];                          // (greater, equal) in this slice
+  __shared__ float red_m[kSelThreads / 32][kGroup], red_s[kSelThreads / 32][kGroup];
+  __shared__ float zl[kGroup];
   __shared__ int scan_buf[32];
   __shared__ uint32_t sh_prefix;
-  __shared__ int sh_remaining;
+  __shared__ int sh_rem, sh_before[2];
 
-  const int unit = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int unit = blockIdx.y;              // (request, KV head)
   const int b = unit / p.H_kv, h = unit % p.H_kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L = p.seq_lens[b];
   int32_t* sel = p.selected + (int64_t)unit * p.budget;
+  // every CTA of a cluster takes the same early exit (same unit)
   if (L < 0 || (L + kPage - 1) / kPage > p.max_pages) {
-    if (tid == 0) {
+    if (tid == 0 && rank == 0) {
       p.n_selected[unit] = 0;
       if (h == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
     }
@@ -406,96 +490,129 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   }
   const int n = L / kPage;
   const int kk = min(p.budget, n);
+  const int j0 = (int)(((long long)n * rank) / kSelCluster);
+  const int j1 = (int)(((long long)n * (rank + 1)) / kSelCluster);
+  const int len = j1 - j0;
   if (n <= p.budget) {   // every full page is selected
-    for (int j = tid; j < n; j += blockDim.x) sel[j] = j;
-    if (tid == 0) p.n_selected[unit] = n;
+    for (int j = j0 + tid; j < j1; j += blockDim.x) sel[j] = j;
+    if (tid == 0 && rank == 0) p.n_selected[unit] = n;
     return;
   }
 
-  // ---- Z_g: combine the scoring pass's partial log-sum-exps
+  // ---- Z_g (log2 units) from the scoring pass's partials of this unit
   {
-    float m[kGroup], s[kGroup];
+    const int hg = h / p.h_cta, hl = h % p.h_cta;
+    const long long u = (long long)b * p.head_groups + hg;
+    const long long ub = u * p.n_chunks, ue = ub + p.n_chunks - 1;   // first / last item
+    long long cf = (ub * p.score_grid) / p.n_items;
+    while (cf + 1 < p.score_grid && score_item_begin(p, (int)cf + 1) <= ub) ++cf;
+    while (cf > 0 && score_item_begin(p, (int)cf) > ub) --cf;
+    long long cl = (ue * p.score_grid) / p.n_items;
+    while (cl + 1 < p.score_grid && score_item_begin(p, (int)cl + 1) <= ue) ++cl;
+    while (cl > 0 && score_item_begin(p, (int)cl) > ue) --cl;
+    float m[kGroup], sm[kGroup];
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       m[g] = -INFINITY;
-      s[g] = 0.f;
+      sm[g] = 0.f;
     }
-    const int nparts = p.n_chunks * p.wph;
-    const float* part = p.partials + (int64_t)unit * nparts * kGroup * 2;
-    for (int i = tid; i < nparts; i += blockDim.x) {
-#pragma unroll
-      for (int g = 0; g < kGroup; ++g) lse_merge(m[g], s[g], part[(i * kGroup + g) * 2], part[(i * kGroup + g) * 2 + 1]);
+    const int nent = (int)(cl - cf + 1) * p.wph;
+    for (int i = tid; i < nent; i += blockDim.x) {
+      const int c = (int)cf + i / p.wph, sub = i % p.wph;
+      const int seg = (int)(u - score_item_begin(p, c) / p.n_chunks);
+      const int w = hl * p.wph + sub;
+      const float4* part = reinterpret_cast<const float4*>(
+          p.partials + (((int64_t)c * p.seg_slots + seg) * 8 + w) * kGroup * 2);
+      const float4 a = part[0], c2 = part[1];
+      lse_merge(m[0], sm[0], a.x, a.y);
+      lse_merge(m[1], sm[1], a.z, a.w);
+      lse_merge(m[2], sm[2], c2.x, c2.y);
+      lse_merge(m[3], sm[3], c2.z, c2.w);
     }
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m[g], o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s[g], o);
-        lse_merge(m[g], s[g], m2, s2);
+        const float s2 = __shfl_xor_sync(0xffffffffu, sm[g], o);
+        lse_merge(m[g], sm[g], m2, s2);
       }
       if (lane == 0) {
         red_m[warp][g] = m[g];
-        red_s[warp][g] = s[g];
+        red_s[warp][g] = sm[g];
       }
     }
     __syncthreads();
     if (tid < kGroup) {
       float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) lse_merge(mm, ss, red_m[w][tid], red_s[w][tid]);
-      zg[tid] = mm + logf(ss);
+      for (int w = 0; w < kSelThreads / 32; ++w) lse_merge(mm, ss, red_m[w][tid], red_s[w][tid]);
+      zl[tid] = (mm + logf(ss)) * kLog2e;
     }
     __syncthreads();
   }
 
-  // ---- shared table: mean over the group's heads of exp(s - Z_g); keys are
-  // the fp32 bit patterns (non-negative floats order like unsigned ints).
-  uint32_t* keys = p.keys + (int64_t)unit * p.max_pages;
-  const float* srow = p.scores + (int64_t)unit * p.max_pages * kGroup;
-  const float z0 = zg[0], z1 = zg[1], z2 = zg[2], z3 = zg[3];
-  for (int j = tid; j < n; j += blockDim.x) {
-    const float4 sv = *reinterpret_cast<const float4*>(srow + (int64_t)j * kGroup);
-    float avg = 0.25f * (expf(sv.x - z0) + expf(sv.y - z1) + expf(sv.z - z2) + expf(sv.w - z3));
-    if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
-    keys[j] = __float_as_uint(avg);
+  // ---- keys of this slice: mean over the group's heads of exp(s - Z_g), as
+  // fp32 bit patterns (non-negative floats order like unsigned ints)
+  {
+    const float4* srow = reinterpret_cast<const float4*>(p.scores + (int64_t)unit * p.max_pages * kGroup);
+    const float z0 = zl[0], z1 = zl[1], z2 = zl[2], z3 = zl[3];
+#pragma unroll 4
+    for (int i = tid; i < len; i += blockDim.x) {
+      const float4 sv = srow[j0 + i];
+      float avg = 0.25f * (fast_exp2(sv.x * kLog2e - z0) + fast_exp2(sv.y * kLog2e - z1) +
+                           fast_exp2(sv.z * kLog2e - z2) + fast_exp2(sv.w * kLog2e - z3));
+      if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
+      keys_s[i] = __float_as_uint(avg);
+    }
+  }
+  if (tid == 0) {
+    sh_prefix = 0;
+    sh_rem = kk;
   }
   __syncthreads();
 
-  // ---- radix select (8-bit digits, MSB first) of the kk-th largest key
-  if (tid == 0) {
-    sh_prefix = 0;
-    sh_remaining = kk;
-  }
+  // ---- radix select over the whole cluster's keys
   for (int pass = 0; pass < 4; ++pass) {
+    const int buf = pass & 1;
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
     const uint32_t prefix = sh_prefix;
     const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int j = tid; j < n; j += blockDim.x) {
-      const uint32_t k = keys[j];
-      if ((k & hmask) == (prefix & hmask)) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    hist[buf][tid] = 0;   // kSelThreads == 256 bins
+    __syncthreads();
+    for (int base = tid & ~31; base < len; base += blockDim.x) {
+      const int i = base + lane;
+      uint32_t k = 0;
+      bool match = false;
+      if (i < len) {
+        k = keys_s[i];
+        match = (k & hmask) == (prefix & hmask);
+      }
+      hist_add(hist[buf], (k >> shift) & 255u, match);
     }
+    cluster.sync();   // every CTA's histogram of this pass is complete
+    int sum = 0;
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) sum += *cluster.map_shared_rank(&hist[buf][tid], r);
+    tot[tid] = sum;
     __syncthreads();
     if (warp == 0) {
       // lane l owns digits [8l, 8l+8); find the digit holding the remaining-th
-      // largest key, scanning from the top.
-      int c[8], tot = 0;
+      // largest key, scanning from the top
+      int c[8], lt = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        c[i] = hist[8 * lane + i];
-        tot += c[i];
+        c[i] = tot[8 * lane + i];
+        lt += c[i];
       }
-      int above = tot;   // inclusive suffix sum over lanes >= lane
+      int above = lt;   // inclusive suffix sum over lanes >= lane
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_down_sync(0xffffffffu, above, o);
         if (lane + o < 32) above += y;
       }
-      const int strictly_above = above - tot;   // keys in lanes > lane
-      const int rem = sh_remaining;
-      const bool mine = strictly_above < rem && above >= rem;
-      if (mine) {
+      const int strictly_above = above - lt;
+      const int rem = sh_rem;
+      if (strictly_above < rem && above >= rem) {
         int acc = strictly_above;
         int digit = 8 * lane;
 #pragma unroll
@@ -507,38 +624,58 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
           acc += c[i];
         }
         sh_prefix = prefix | ((uint32_t)digit << shift);
-        sh_remaining = rem - acc;
+        sh_rem = rem - acc;
       }
     }
     __syncthreads();
   }
   const uint32_t T = sh_prefix;
-  const int eq_take = sh_remaining;   // keys equal to T to take, lowest index first
+  const int eq_take = sh_rem;   // keys equal to T to take, lowest page index first
 
   // ---- compaction in ascending page order
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+  const int per = (len + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(len, tid * per), c1 = min(len, c0 + per);
   int gt = 0, eq = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t k = keys[j];
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = keys_s[i];
     gt += k > T;
     eq += k == T;
   }
-  int eq_total;
-  const int eq_before = block_exclusive_scan(eq, scan_buf, eq_total);
-  const int take = max(0, min(eq, eq_take - eq_before));
-  int sel_total;
-  int pos = block_exclusive_scan(gt + take, scan_buf, sel_total);
+  int gt_slice, eq_slice;
+  const int gt_before = block_exclusive_scan(gt, scan_buf, gt_slice);
+  const int eq_before = block_exclusive_scan(eq, scan_buf, eq_slice);
+  if (tid == 0) {
+    slice_cnt[0] = gt_slice;
+    slice_cnt[1] = eq_slice;
+  }
+  cluster.sync();   // every slice's counts are published
+  if (tid == 0) {
+    int g = 0, e = 0;
+    for (int r = 0; r < rank; ++r) {
+      const int* rc = cluster.map_shared_rank(slice_cnt, r);
+      g += rc[0];
+      e += rc[1];
+    }
+    sh_before[0] = g;
+    sh_before[1] = e;
+  }
+  __syncthreads();
+  const int eq_lower = sh_before[1];                      // equal keys in lower slices
+  const int taken_lower = min(eq_lower, eq_take);
+  const int take = max(0, min(eq, eq_take - eq_lower - eq_before));
+  const int take_before = max(0, min(eq_before, eq_take - eq_lower));
+  int pos = sh_before[0] + taken_lower + gt_before + take_before;
   int taken = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t k = keys[j];
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = keys_s[i];
     if (k > T || (k == T && taken < take)) {
       if (k == T) ++taken;
-      if (pos < kk) sel[pos] = j;
+      if (pos < kk) sel[pos] = j0 + i;
       ++pos;
     }
   }
-  if (tid == 0) p.n_selected[unit] = kk;
+  if (tid == 0 && rank == 0) p.n_selected[unit] = kk;
+  cluster.sync();   // no CTA leaves while another may still read its counts
 }
 
 }  // namespace locks
@@ -558,7 +695,16 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream) {
-  select_kernel<<<units, kSelThreads, 0, stream>>>(p);
+  // dynamic shared memory: one slice of keys (checked against the limit on the host)
+  const size_t dyn = (size_t)((p.max_pages + kSelCluster - 1) / kSelCluster) * sizeof(uint32_t);
+  static size_t attr_bytes = 0;
+  if (dyn > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    attr_bytes = dyn;
+  }
+  dim3 grid(kSelCluster, units);
+  select_kernel<<<grid, kSelThreads, dyn, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,85 @@
+"""GPU parity on the five named workloads at full size, in the launch
+configuration bench.py times.  The oracle checks every unit where that is
+cheap and sampled (request, KV head) units where the cache is too large to
+check whole (batch 16: 4 requests x 8 heads; batch 64: 3 requests x 8 heads);
+the builder is checked on sampled pages."""
+
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from sparse_long_context_locks_gb300 import workload as W
+
+from gpu_helpers import Run, check_records, check_unit
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_build_sample(run, b, h, n_pages, rng):
+    n = run.lens[b] // 16
+    pages = np.sort(rng.choice(n, size=min(n_pages, n), replace=False))
+    K = run.pages_f64(run.d["k_cache"], b, h, pages)
+    blocks = torch.from_numpy(run.bt[b, pages].astype(np.int64)).cuda()
+    rec = run.summ[blocks, h].cpu().numpy()
+    return check_records(rec, K)
+
+
+def _free(run):
+    del run.d, run.summ, run.bufs
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_pr1_4k():
+    run = Run(W.CONFIGS["pr1_4k"], dense=True)
+    assert run.status == 0
+    check_unit(run, 0, 0)
+
+
+def test_llama8b_128k_all_heads():
+    run = Run(W.CONFIGS["llama8b_128k"])
+    assert run.status == 0
+    rng = np.random.default_rng(0)
+    for h in range(8):
+        check_unit(run, 0, h)
+    _check_build_sample(run, 0, 3, 1024, rng)
+    _free(run)
+
+
+def test_batch16_32k_sampled_requests():
+    w = W.CONFIGS["batch16_32k"]
+    run = Run(w, tail_fill="nan")
+    assert run.status == 0
+    assert len(set(run.lens)) > 1
+    for b in (0, 5, 10, 15):
+        for h in range(8):
+            check_unit(run, b, h)
+    _free(run)
+
+
+def test_ctx1m_all_heads():
+    run = Run(W.CONFIGS["ctx1m"])
+    assert run.status == 0
+    rng = np.random.default_rng(1)
+    for h in range(8):
+        check_unit(run, 0, h, check_scores_too=(h in (0, 5)))
+    _check_build_sample(run, 0, 6, 2048, rng)
+    lens = run.lens
+    by = W.algorithmic_bytes(lens, 8, 4, run.w.budget_pages)
+    assert by["dense_kv"] / (by["score"] + by["sparse_kv"]) >= 9.0
+    _free(run)
+
+
+@pytest.mark.parametrize("regime", ["batch64_256k_lowrank", "batch64_256k_fullrank"])
+def test_batch64_256k_sampled_requests(regime):
+    run = Run(W.CONFIGS[regime])
+    assert run.status == 0
+    rng = np.random.default_rng(2)
+    for b in (0, 31, 63):
+        for h in range(8):
+            check_unit(run, b, h, check_scores_too=(h % 4 == 0))
+    _check_build_sample(run, 17, 2, 512, rng)
+    _free(run)
