@@ -1,9 +1,11 @@
 """Decode-step benchmark of the LOCKS hot path on GB300.
 
 A step is one pass of the decode hot path over one batch of synthetic input:
-page scoring + group-shared top-k selection (locks_score_select) followed by
-sparse paged attention over the selected pages and the open tail page
-(locks_sparse_decode), captured once into a CUDA graph and replayed.  The
+locks_decode_step = page scoring (locks_score) followed by the fused cluster
+kernel of locks_select_sparse_decode (group-shared top-k selection and sparse
+paged attention over the selected pages and the open tail page), captured once
+into a CUDA graph and replayed.  The separate selection and split-K sparse
+attention kernels are timed too (rows "select_us", "sparse_attention_us").  The
 summary builder (run when pages are finalised, off the decode critical path)
 and the dense comparator are timed in the same run and reported under "rows".
 
@@ -263,11 +265,9 @@ def main():
     sink = torch.zeros((), device="cuda")
 
     def step_calls(s):
-        L.locks_score_select(H, data["q"], summ, data["block_table"], data["seq_lens"], w.budget_pages,
-                             bufs.selected, bufs.n_selected, bufs.workspace, scores=bufs.scores, stream=s)
-        L.locks_sparse_decode(H, data["q"], data["k_cache"], data["v_cache"], data["block_table"],
-                              data["seq_lens"], bufs.selected, bufs.n_selected, w.budget_pages, bufs.out,
-                              bufs.workspace, stream=s)
+        L.locks_decode_step(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
+                            data["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                            bufs.workspace, scores=bufs.scores, stream=s)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -289,6 +289,10 @@ def main():
                                                        data["block_table"], data["seq_lens"], bufs.selected,
                                                        bufs.n_selected, w.budget_pages, bufs.out,
                                                        bufs.workspace, stream=s))
+    g_fused = capture(lambda s: L.locks_select_sparse_decode(
+        H, data["q"], data["k_cache"], data["v_cache"], data["block_table"], data["seq_lens"],
+        w.budget_pages, bufs.selected, bufs.n_selected, bufs.out, bufs.workspace, scores=bufs.scores,
+        stream=s))
     dense_out = torch.empty_like(bufs.out)
     g_dense = capture(lambda s: L.locks_dense_decode(H, data["q"], data["k_cache"], data["v_cache"],
                                                      data["block_table"], data["seq_lens"], dense_out,
@@ -348,6 +352,7 @@ def main():
         return tot / reps * 1e3   # us
 
     us_score = time_graph(g_score)
+    us_fused = time_graph(g_fused)
     us_select = time_graph(g_select)
     us_sparse = time_graph(g_sparse)
     us_dense = time_graph(g_dense, reps=max(10, R // 4))
@@ -419,14 +424,15 @@ def main():
         "clocks": ClockSampler.summary(clock_rows),
         "e2e": {"value": w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "mode": "pinned H2D of q and seq_lens, graph replay of the two C-ABI calls, "
+                "mode": "pinned H2D of q and seq_lens, graph replay of locks_decode_step, "
                         "D2H of out, host wall clock incl. stream sync"},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs, "peak": peak,
                      "unit": "GB/s", "frac": score_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": by["score"], "peak_source": peak_src},
         "rows": {
-            "score_us": us_score, "select_us": us_select, "sparse_attention_us": us_sparse,
+            "score_us": us_score, "select_attend_fused_us": us_fused,
+            "select_us": us_select, "sparse_attention_us": us_sparse,
             "step_us": ms_step * 1e3,
             "step_GBps": by["step"] / (ms_step * 1e-3) / 1e9,
             "sparse_attention_GBps": by["sparse_kv"] / (us_sparse * 1e-6) / 1e9,

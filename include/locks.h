@@ -186,6 +186,34 @@ locks_status locks_sparse_decode(const locks_cfg *cfg, const void *q, const void
                                  float sm_scale, float *out, void *workspace,
                                  size_t workspace_bytes, locks_stream_t stream);
 
+/* Selection and sparse attention fused, §2 "Reconstruction and selection",
+ * "Group-shared selection (GQA)" and the implementation note that scoring,
+ * selection and sparse attention run back to back with no host round trip:
+ * the same results as locks_select followed by locks_sparse_decode (it writes
+ * `selected`, `n_selected` and `out`), computed by one thread-block cluster of
+ * 8 CTAs per (request, KV head) that keeps the selection on chip and merges
+ * the split attention through distributed shared memory.  It is launched as a
+ * programmatic dependent of the preceding kernel on `stream` (normally
+ * locks_score), so its set-up overlaps that kernel's tail.  Needs
+ * budget_pages <= 2047 and max_pages <= 131072, else LOCKS_ERR_UNSUPPORTED. */
+locks_status locks_select_sparse_decode(const locks_cfg *cfg, const void *q, const void *k_cache,
+                                        const void *v_cache, int64_t num_blocks,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        int32_t batch, int32_t max_pages, int32_t budget_pages,
+                                        const float *scores, int32_t *selected, int32_t *n_selected,
+                                        float sm_scale, float *out, void *workspace,
+                                        size_t workspace_bytes, locks_stream_t stream);
+
+/* One whole LOCKS decode step for a batch: locks_score then
+ * locks_select_sparse_decode on `stream` (two kernels, the second a
+ * programmatic dependent of the first).  Same limits as the fused call. */
+locks_status locks_decode_step(const locks_cfg *cfg, const void *q, const void *summaries,
+                               const void *k_cache, const void *v_cache, int64_t num_blocks,
+                               const int32_t *block_table, const int32_t *seq_lens, int32_t batch,
+                               int32_t max_pages, int32_t budget_pages, float sm_scale, float *scores,
+                               int32_t *selected, int32_t *n_selected, float *out, void *workspace,
+                               size_t workspace_bytes, locks_stream_t stream);
+
 /* Dense comparator (the full-cache attention LOCKS is measured against):
  * the same computation over every cached token of each request. */
 locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void *k_cache,

@@ -66,9 +66,8 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   const int64_t items = (int64_t)batch * pl.head_groups * pl.n_chunks;
   pl.n_items = (int)items;
   pl.score_grid = (int)(items < kTargetCtas ? items : kTargetCtas);
-  // a CTA's contiguous item range touches at most this many units
-  const int64_t per_cta = (items + pl.score_grid - 1) / pl.score_grid;
-  pl.seg_slots = (int)((per_cta + pl.n_chunks - 1) / pl.n_chunks + 1);
+  // most scoring CTAs one (request, head group) unit's items can span
+  pl.seg_slots = (int)(((int64_t)pl.n_chunks * pl.score_grid + items - 1) / items + 2);
   const int units = batch * H;
   pl.sparse_splits = pick_splits(units, budget + 1);
   pl.sparse_ips = ceil_div(budget + 1, pl.sparse_splits);
@@ -82,7 +81,7 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   pl.off_tickets = off;
   off = align_up(off + (size_t)units * sizeof(uint32_t));
   pl.off_partials = off;
-  off = align_up(off + (size_t)pl.score_grid * pl.seg_slots * 8 * kGroup * 2 * sizeof(float));
+  off = align_up(off + (size_t)batch * pl.head_groups * pl.seg_slots * 8 * kGroup * 2 * sizeof(float));
   pl.off_scores = off;
   off = align_up(off + (size_t)batch * H * max_pages * kGroup * sizeof(float));
   pl.off_attn = off;   // last: its size depends on the split counts
@@ -284,23 +283,14 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t batch, int32_t max_pages,
-                          int32_t budget_pages, const float* scores, int32_t* selected,
-                          int32_t* n_selected, void* workspace, size_t workspace_bytes,
-                          locks_stream_t stream) {
-  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
-  if (batch < 0 || max_pages < 1 || budget_pages < 0) return LOCKS_ERR_INVALID_ARG;
-  if (batch == 0) return LOCKS_OK;
-  LOCKS_CHECK_PTR(seq_lens);
-  LOCKS_CHECK_PTR(n_selected);
-  LOCKS_CHECK_PTR(workspace);
-  if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
-  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
-  if ((max_pages + kSelCluster - 1) / kSelCluster > kSelMaxKeysPerCta) return LOCKS_ERR_UNSUPPORTED;
-  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
-  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+}  // extern "C"
+
+namespace {
+
+void fill_select(SelectParams& p, const Plan& pl, const locks_cfg* cfg, const int32_t* seq_lens, int32_t batch,
+                 int32_t max_pages, int32_t budget_pages, const float* scores, int32_t* selected,
+                 int32_t* n_selected, void* workspace) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  SelectParams p{};
   p.seq_lens = seq_lens;
   p.scores = scores ? scores : reinterpret_cast<const float*>(ws + pl.off_scores);
   p.partials = reinterpret_cast<const float*>(ws + pl.off_partials);
@@ -318,7 +308,96 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   p.head_groups = pl.head_groups;
   p.h_cta = pl.h_cta;
   p.wph = pl.wph;
+}
+
+}  // namespace
+
+extern "C" {
+
+locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                          int32_t budget_pages, const float* scores, int32_t* selected,
+                          int32_t* n_selected, void* workspace, size_t workspace_bytes,
+                          locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(n_selected);
+  LOCKS_CHECK_PTR(workspace);
+  if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  if (select_smem_bytes(max_pages, budget_pages) > (size_t)kSmemLimit) return LOCKS_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  SelectParams p{};
+  fill_select(p, pl, cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected, workspace);
   return from_cuda(launch_select(p, batch * cfg->num_kv_heads, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_select_sparse_decode(const locks_cfg* cfg, const void* q, const void* k_cache,
+                                        const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                                        const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                                        int32_t budget_pages, const float* scores, int32_t* selected,
+                                        int32_t* n_selected, float sm_scale, float* out, void* workspace,
+                                        size_t workspace_bytes, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f)) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(q);
+  LOCKS_CHECK_PTR(k_cache);
+  LOCKS_CHECK_PTR(v_cache);
+  LOCKS_CHECK_PTR(block_table);
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(n_selected);
+  LOCKS_CHECK_PTR(out);
+  LOCKS_CHECK_PTR(workspace);
+  if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  const int H = cfg->num_kv_heads;
+  // one cluster per (request, KV head): its 64 warps take at most 32 items
+  // each, and its 8 slices of keys fit in the 128 KB staging ring
+  if (budget_pages > kFusedMaxBudget || (max_pages + kSelCluster - 1) / kSelCluster > kFusedMaxKeysPerCta ||
+      fused_smem_bytes(max_pages, budget_pages) > (size_t)kSmemLimit)
+    return LOCKS_ERR_UNSUPPORTED;
+  if (num_blocks * H * kPage >= (int64_t)1 << 31) return LOCKS_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  CUtensorMap tmk, tmv;
+  if (!encode_cache_map(&tmk, k_cache, num_blocks, H) || !encode_cache_map(&tmv, v_cache, num_blocks, H))
+    return LOCKS_ERR_CUDA;
+  FusedParams p{};
+  fill_select(p.sel, pl, cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected, workspace);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_table = block_table;
+  p.out = out;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  return from_cuda(launch_select_attend(tmk, tmv, p, batch * H, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* summaries, const void* k_cache,
+                               const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                               const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                               float sm_scale, float* scores, int32_t* selected, int32_t* n_selected, float* out,
+                               void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (budget_pages < 0 || budget_pages > kFusedMaxBudget) return budget_pages < 0 ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch > 0 && (max_pages + kSelCluster - 1) / kSelCluster > kFusedMaxKeysPerCta) return LOCKS_ERR_UNSUPPORTED;
+  if (batch > 0) {
+    LOCKS_CHECK_PTR(k_cache);
+    LOCKS_CHECK_PTR(v_cache);
+    LOCKS_CHECK_PTR(n_selected);
+    LOCKS_CHECK_PTR(out);
+    if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
+    if (!(sm_scale > 0.f)) return LOCKS_ERR_INVALID_ARG;
+  }
+  locks_status st = locks_score(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores,
+                                workspace, workspace_bytes, stream);
+  if (st != LOCKS_OK) return st;
+  return locks_select_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, batch, max_pages,
+                                    budget_pages, scores, selected, n_selected, sm_scale, out, workspace,
+                                    workspace_bytes, stream);
 }
 
 locks_status locks_score_select(const locks_cfg* cfg, const void* q, const void* summaries,

@@ -24,7 +24,35 @@ constexpr int kGroup = 4;
 constexpr int kRecord = 784;
 constexpr int kTargetCtas = 304;   // 2 resident CTAs x 152 SMs (GB300)
 constexpr int kSelCluster = 8;     // CTAs per (request, KV head) in the selection
-constexpr int kSelMaxKeysPerCta = 50000;   // 200 KB of keys in shared memory
+constexpr int kFusedMaxKeysPerCta = 16384; // fused pass: keys + block ids share the 128 KB ring
+constexpr int kFusedMaxBudget = 2047;      // fused pass: <= 32 items per warp of 64
+constexpr int kSmemLimit = 216 * 1024;     // dynamic shared memory we allow a CTA (static <= 11 KB)
+
+// Entries per CTA in rank 0's candidate arrays (key, page, block: 12 bytes
+// each, kSelCluster segments).  At least min(budget, slice) so that an exact
+// local top-k always fits; up to 2 budget + 64 so that a slice's whole
+// boundary histogram bin usually fits, as far as kSmemLimit leaves room
+// after `fixed` bytes of other dynamic shared memory.
+__host__ __device__ inline int sel_cand_stride(int max_pages, int budget, size_t fixed) {
+  const int slice_cap = (max_pages + kSelCluster - 1) / kSelCluster;
+  const int lo = budget < slice_cap ? budget : slice_cap;
+  long long hi = 2LL * budget + 64;
+  if (hi > slice_cap) hi = slice_cap;
+  const long long fit = fixed < (size_t)kSmemLimit ? (long long)(kSmemLimit - fixed) / (12 * kSelCluster) : 0;
+  if (hi > fit) hi = fit;
+  return hi > lo ? (int)hi : lo;
+}
+
+// Dynamic shared memory of the selection kernel: slice keys, the selected
+// list, then C candidate segments (key, page, block).
+__host__ __device__ inline size_t select_fixed_bytes(int max_pages, int budget) {
+  const int slice_cap = (max_pages + kSelCluster - 1) / kSelCluster;
+  return 4 * ((size_t)slice_cap + (size_t)budget + 4);
+}
+__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget) {
+  const size_t fixed = select_fixed_bytes(max_pages, budget);
+  return fixed + 12 * (size_t)kSelCluster * sel_cand_stride(max_pages, budget, fixed);
+}
 
 // ---------------------------------------------------------------- status
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bit) {

@@ -23,6 +23,7 @@
 
 #include <cstdint>
 
+#include "attn_tile.cuh"
 #include "common.cuh"
 #include "params.h"
 
@@ -32,18 +33,9 @@ namespace locks {
 constexpr int kAttnWarps = 4;
 constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kAttnStages = 3;
-constexpr int kTileBytes = kPage * kHeadDim * 2;           // 4096: one page-head of K (or V)
-constexpr int kStageBytes = 2 * kTileBytes;                // K + V
 constexpr int kAttnRing = kAttnWarps * kAttnStages * kStageBytes;
 constexpr int kAttnSmem = kAttnRing + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kPartStride = 2 + kHeadDim;
-
-// Swizzled (128B) address of 16-byte chunk `chunk` (0..15 across the 128
-// columns) of row `row` of a K/V tile made of two 64-column boxes.
-__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int row, int chunk) {
-  const int half = chunk >> 3, c = chunk & 7;
-  return tile + half * 2048 + row * 128 + ((c ^ (row & 7)) << 4);
-}
 
 __device__ __forceinline__ void unit_items(const AttnParams& p, int b, int h, int& n, int& t,
                                            int& nsel, int& items) {
@@ -97,7 +89,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kAttnRing);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, t4 = lane & 3;
   const int unit = blockIdx.y, split = blockIdx.x;
   const int b = unit / p.H_kv, h = unit % p.H_kv;
 
@@ -131,18 +122,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     item_block(p, b, h, my_first + (32 + lane) * kAttnWarps, n, tail, nsel, nxt_blk, nxt_valid);
 
   auto issue = [&](int64_t blk, int stage) {
-    uint64_t* bar = &mybar[stage];
-    uint8_t* dst = ring_ptr + stage * kStageBytes;
-    if (blk >= 0) {
-      mbar_arrive_expect_tx(bar, kStageBytes);
-      const int32_t y = (int32_t)((blk * p.H_kv + h) * kPage);
-      tma_load_2d(dst, &tmk, 0, y, bar);
-      tma_load_2d(dst + 2048, &tmk, 64, y, bar);
-      tma_load_2d(dst + kTileBytes, &tmv, 0, y, bar);
-      tma_load_2d(dst + kTileBytes + 2048, &tmv, 64, y, bar);
-    } else {
-      mbar_arrive(bar);   // nothing to load: complete the phase at once
-    }
+    attn_issue_page(&tmk, &tmv, ring_ptr + stage * kStageBytes, &mybar[stage], blk, p.H_kv, h);
   };
 
   // prologue: lane k issues item k into stage k
@@ -151,94 +131,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     issue(cur_blk, lane);
   }
 
-  // B operand of S = K q^T: column n = head n & 3 of the group.
   uint32_t qb[8][2];
-  {
-    const __nv_bfloat16* qh = p.q + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup + (gid & 3)) * kHeadDim;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      qb[s][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * t4);
-      qb[s][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * s + 2 * t4 + 8);
-    }
-  }
+  attn_load_q(qb, p.q + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup) * kHeadDim, lane);
   __syncwarp();
 
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  PageAttnState st;
+  attn_init(st);
   bool ok = true;
 
   for (int k = 0; k < my_count; ++k) {
     const int stage = k % kAttnStages;
     if (ok) ok = mbar_wait(&mybar[stage], (k / kAttnStages) & 1, p.status);
     const int valid = stage_valid[warp][stage];
-    const uint32_t ktile = ring + stage * kStageBytes;
-    const uint32_t vtile = ktile + kTileBytes;
-
-    if (ok && valid > 0) {
-      if (valid < kPage) {
-        // tail page: zero the V rows past the valid tokens (they may hold
-        // anything, and 0 * NaN would poison the accumulator)
-        uint8_t* vp = ring_ptr + stage * kStageBytes + kTileBytes;
-        for (int idx = lane; idx < (kPage - valid) * 16; idx += 32) {
-          const int row = valid + idx / 16, chunk = idx % 16;
-          const int half = chunk >> 3, c = chunk & 7;
-          *reinterpret_cast<uint4*>(vp + half * 2048 + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // ---- S = K q^T (rows = tokens, cols = heads)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int lchk = lane >> 4;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, tile_addr(ktile, lrow, 2 * ks + lchk));
-        mma_bf16(s, a[0], a[1], a[2], a[3], qb[ks][0], qb[ks][1]);
-      }
-      // scale into log2 units, mask invalid tokens
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s[i] *= p.scale_log2;
-      if (gid >= valid) s[0] = s[1] = -INFINITY;
-      if (gid + 8 >= valid) s[2] = s[3] = -INFINITY;
-      // ---- online softmax, per column (2t4, 2t4+1)
-      float mt0 = fmaxf(s[0], s[2]), mt1 = fmaxf(s[1], s[3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
-        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
-      }
-      const float mn0 = fmaxf(m_run[0], mt0), mn1 = fmaxf(m_run[1], mt1);
-      const float al0 = fast_exp2(m_run[0] - mn0), al1 = fast_exp2(m_run[1] - mn1);
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-      const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
-      const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
-      l_run[0] = l_run[0] * al0 + p0 + p2;
-      l_run[1] = l_run[1] * al1 + p1 + p3;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        acc[i][0] *= al0;
-        acc[i][1] *= al1;
-        acc[i][2] *= al0;
-        acc[i][3] *= al1;
-      }
-      // P^T as the B operand (k = tokens, n = heads)
-      const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-      const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
-      // ---- O^T[dim][head] += V^T P
-      const int vrow = (lane & 7) + (lane >> 4) * 8;
-      const int vsel = (lane >> 3) & 1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t a[4];
-        ldsm_x4_trans(a, tile_addr(vtile, vrow, 2 * i + vsel));
-        mma_bf16(acc[i], a[0], a[1], a[2], a[3], pb0, pb1);
-      }
-    }
+    if (ok && valid > 0)
+      attn_page(st, ring + stage * kStageBytes, ring_ptr + stage * kStageBytes + kTileBytes, valid, qb,
+                p.scale_log2, lane);
     // order this warp's generic smem accesses before the next async write
     fence_proxy_async_smem();
     __syncwarp();
@@ -263,34 +170,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     __syncwarp();
   }
 
-  // ---- reduce l over the 8 token rows (lanes with equal t4)
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], o);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], o);
-  }
+  attn_finish(st);
 
   // ---- merge the 4 warps through shared memory (ring no longer in use)
   __syncthreads();
   float* wO = reinterpret_cast<float*>(smem);                       // [warp][G][128]
   float* wM = wO + kAttnWarps * kGroup * kHeadDim;                  // [warp][G]
   float* wL = wM + kAttnWarps * kGroup;                             // [warp][G]
-  if (t4 < 2) {   // columns 2t4, 2t4+1 are heads 0..3
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int d0 = 16 * i + gid, d1 = d0 + 8;
-      wO[(warp * kGroup + 2 * t4) * kHeadDim + d0] = acc[i][0];
-      wO[(warp * kGroup + 2 * t4 + 1) * kHeadDim + d0] = acc[i][1];
-      wO[(warp * kGroup + 2 * t4) * kHeadDim + d1] = acc[i][2];
-      wO[(warp * kGroup + 2 * t4 + 1) * kHeadDim + d1] = acc[i][3];
-    }
-    if (gid == 0) {
-      wM[warp * kGroup + 2 * t4] = m_run[0];
-      wM[warp * kGroup + 2 * t4 + 1] = m_run[1];
-      wL[warp * kGroup + 2 * t4] = l_run[0];
-      wL[warp * kGroup + 2 * t4 + 1] = l_run[1];
-    }
-  }
+  attn_store_warp(st, wO + warp * kGroup * kHeadDim, wM + warp * kGroup, wL + warp * kGroup, lane);
   __syncthreads();
 
   const int d = threadIdx.x;   // 128 threads = 128 dims

@@ -15,7 +15,7 @@ struct ScoreParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* scores;      // [batch][H_kv][max_pages][G]
-  float* partials;    // [grid][seg_slots][8 warps][G][2]: one LSE partial per unit segment
+  float* partials;    // [batch*head_groups][seg_slots][8 warps][G][2]: LSE partial per covering CTA
   uint32_t* status;
   int64_t num_blocks;
   int batch, max_pages, H_kv;
@@ -26,7 +26,7 @@ struct ScoreParams {
   int n_chunks;       // chunks per (b, head group)
   int head_groups;    // H_kv / h_cta
   int n_items;        // batch * head_groups * n_chunks
-  int seg_slots;      // most (request, head group) units one CTA's item range can touch
+  int seg_slots;      // most scoring CTAs one (request, head group) unit's items can span
 };
 
 struct SelectParams {
@@ -67,7 +67,19 @@ struct BuildParams {
   int n_build, H_kv;
 };
 
+struct FusedParams {
+  SelectParams sel;
+  const __nv_bfloat16* q;
+  const int32_t* block_table;
+  float* out;                  // [batch][H_kv*G][128]
+  int64_t num_blocks;
+  float scale_log2;            // sm_scale * log2(e)
+};
+
 cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_select_attend(const CUtensorMap& tmk, const CUtensorMap& tmv, const FusedParams& p,
+                                 int units, cudaStream_t stream);
+size_t fused_smem_bytes(int max_pages, int budget);
 cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream);
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream);

@@ -26,9 +26,7 @@
 
 #include "common.cuh"
 #include "params.h"
-
-#include <cooperative_groups.h>
-namespace cg = cooperative_groups;
+#include "cluster_select.cuh"
 
 namespace locks {
 
@@ -191,20 +189,6 @@ __device__ __forceinline__ void lse_push(float& m, float& s, float x) {
   m = mn;
 }
 
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) {
-    m = m2;
-    s = s2;
-    return;
-  }
-  if (m2 > m) {
-    s = s * fast_exp2((m - m2) * kLog2e) + s2;
-    m = m2;
-  } else {
-    s += s2 * fast_exp2((m2 - m) * kLog2e);
-  }
-}
 
 __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScoreParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -213,6 +197,9 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
   uint64_t* empty = full + kScoreStages;
   uint32_t* live = reinterpret_cast<uint32_t*>(empty + kScoreStages);
 
+  // a programmatic dependent (the fused select + attention pass) may start its
+  // prologue as SMs free up; it waits for this grid's results before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScoreStages; ++s) {
@@ -399,9 +386,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
     const float os = __shfl_xor_sync(0xffffffffu, run_s, 16);
     lse_merge(run_m, run_s, om, os);
     if (t == 0 && gid < 4) {
-      const int seg = unit - first_unit;
+      // slot: this CTA's index among the CTAs covering the unit
+      const int slot = (int)blockIdx.x - score_cta_of((long long)unit * p.n_chunks, p.n_items, gridDim.x);
       float* part = p.partials +
-                    ((((int64_t)blockIdx.x * p.seg_slots + seg) * kScoreConsumers + warp) * kGroup + gid) * 2;
+                    ((((int64_t)unit * p.seg_slots + slot) * kScoreConsumers + warp) * kGroup + gid) * 2;
       part[0] = run_m;
       part[1] = run_s;
     }
@@ -411,271 +399,21 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // ---------------------------------------------------------------- select
 
 
-constexpr int kSelThreads = 256;
-
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_buf[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? warp_buf[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    warp_buf[lane] = w;   // inclusive over warps
-  }
-  __syncthreads();
-  total = warp_buf[nw - 1];
-  const int before = (warp > 0 ? warp_buf[warp - 1] : 0) + x - v;
-  __syncthreads();
-  return before;
-}
-
-// Warp-aggregated shared-memory histogram add: lanes holding the same bin add once.
-__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
-  const uint32_t act = __ballot_sync(0xffffffffu, active);
-  if (active) {
-    const uint32_t peers = __match_any_sync(act, bin);
-    if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (int)__popc(peers));
-  }
-}
-
-// First item of CTA c of the scoring grid.
-__device__ __forceinline__ long long score_item_begin(const SelectParams& p, int c) {
-  return ((long long)c * p.n_items) / p.score_grid;
-}
-
-// One cluster of kSelCluster CTAs per (request, KV head).  CTA r keeps the
-// keys of pages [n r / C, n (r+1) / C) in its shared memory.  A radix select
-// (four 8-bit digits, MSB first) finds the kk-th largest key: each pass every
-// CTA histograms its own keys, one cluster barrier, then every CTA sums the C
-// histograms through distributed shared memory and takes the same digit
-// decision.  Compaction: per-CTA counts exchanged the same way give each CTA
-// its output offset, so indices come out in ascending page order.
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
     select_kernel(const SelectParams p) {
-  extern __shared__ __align__(16) uint32_t keys_s[];   // this CTA's slice of keys
-  __shared__ int hist[2][256];
-  __shared__ int tot[256];
-  __shared__ int slice_cnt[2];                          // (greater, equal) in this slice
-  __shared__ float red_m[kSelThreads / 32][kGroup], red_s[kSelThreads / 32][kGroup];
-  __shared__ float zl[kGroup];
-  __shared__ int scan_buf[32];
-  __shared__ uint32_t sh_prefix;
-  __shared__ int sh_rem, sh_before[2];
-
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int unit = blockIdx.y;              // (request, KV head)
-  const int b = unit / p.H_kv, h = unit % p.H_kv;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int L = p.seq_lens[b];
-  int32_t* sel = p.selected + (int64_t)unit * p.budget;
-  // every CTA of a cluster takes the same early exit (same unit)
-  if (L < 0 || (L + kPage - 1) / kPage > p.max_pages) {
-    if (tid == 0 && rank == 0) {
-      p.n_selected[unit] = 0;
-      if (h == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
-    }
-    return;
-  }
-  const int n = L / kPage;
-  const int kk = min(p.budget, n);
-  const int j0 = (int)(((long long)n * rank) / kSelCluster);
-  const int j1 = (int)(((long long)n * (rank + 1)) / kSelCluster);
-  const int len = j1 - j0;
-  if (n <= p.budget) {   // every full page is selected
-    for (int j = j0 + tid; j < j1; j += blockDim.x) sel[j] = j;
-    if (tid == 0 && rank == 0) p.n_selected[unit] = n;
-    return;
-  }
-
-  // ---- Z_g (log2 units) from the scoring pass's partials of this unit
-  {
-    const int hg = h / p.h_cta, hl = h % p.h_cta;
-    const long long u = (long long)b * p.head_groups + hg;
-    const long long ub = u * p.n_chunks, ue = ub + p.n_chunks - 1;   // first / last item
-    long long cf = (ub * p.score_grid) / p.n_items;
-    while (cf + 1 < p.score_grid && score_item_begin(p, (int)cf + 1) <= ub) ++cf;
-    while (cf > 0 && score_item_begin(p, (int)cf) > ub) --cf;
-    long long cl = (ue * p.score_grid) / p.n_items;
-    while (cl + 1 < p.score_grid && score_item_begin(p, (int)cl + 1) <= ue) ++cl;
-    while (cl > 0 && score_item_begin(p, (int)cl) > ue) --cl;
-    float m[kGroup], sm[kGroup];
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      m[g] = -INFINITY;
-      sm[g] = 0.f;
-    }
-    const int nent = (int)(cl - cf + 1) * p.wph;
-    for (int i = tid; i < nent; i += blockDim.x) {
-      const int c = (int)cf + i / p.wph, sub = i % p.wph;
-      const int seg = (int)(u - score_item_begin(p, c) / p.n_chunks);
-      const int w = hl * p.wph + sub;
-      const float4* part = reinterpret_cast<const float4*>(
-          p.partials + (((int64_t)c * p.seg_slots + seg) * 8 + w) * kGroup * 2);
-      const float4 a = part[0], c2 = part[1];
-      lse_merge(m[0], sm[0], a.x, a.y);
-      lse_merge(m[1], sm[1], a.z, a.w);
-      lse_merge(m[2], sm[2], c2.x, c2.y);
-      lse_merge(m[3], sm[3], c2.z, c2.w);
-    }
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m[g], o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, sm[g], o);
-        lse_merge(m[g], sm[g], m2, s2);
-      }
-      if (lane == 0) {
-        red_m[warp][g] = m[g];
-        red_s[warp][g] = sm[g];
-      }
-    }
-    __syncthreads();
-    if (tid < kGroup) {
-      float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < kSelThreads / 32; ++w) lse_merge(mm, ss, red_m[w][tid], red_s[w][tid]);
-      zl[tid] = (mm + logf(ss)) * kLog2e;
-    }
-    __syncthreads();
-  }
-
-  // ---- keys of this slice: mean over the group's heads of exp(s - Z_g), as
-  // fp32 bit patterns (non-negative floats order like unsigned ints)
-  {
-    const float4* srow = reinterpret_cast<const float4*>(p.scores + (int64_t)unit * p.max_pages * kGroup);
-    const float z0 = zl[0], z1 = zl[1], z2 = zl[2], z3 = zl[3];
-#pragma unroll 4
-    for (int i = tid; i < len; i += blockDim.x) {
-      const float4 sv = srow[j0 + i];
-      float avg = 0.25f * (fast_exp2(sv.x * kLog2e - z0) + fast_exp2(sv.y * kLog2e - z1) +
-                           fast_exp2(sv.z * kLog2e - z2) + fast_exp2(sv.w * kLog2e - z3));
-      if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
-      keys_s[i] = __float_as_uint(avg);
-    }
-  }
-  if (tid == 0) {
-    sh_prefix = 0;
-    sh_rem = kk;
-  }
-  __syncthreads();
-
-  // ---- radix select over the whole cluster's keys
-  for (int pass = 0; pass < 4; ++pass) {
-    const int buf = pass & 1;
-    const int shift = 24 - 8 * pass;
-    const uint32_t prefix = sh_prefix;
-    const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    hist[buf][tid] = 0;   // kSelThreads == 256 bins
-    __syncthreads();
-    for (int base = tid & ~31; base < len; base += blockDim.x) {
-      const int i = base + lane;
-      uint32_t k = 0;
-      bool match = false;
-      if (i < len) {
-        k = keys_s[i];
-        match = (k & hmask) == (prefix & hmask);
-      }
-      hist_add(hist[buf], (k >> shift) & 255u, match);
-    }
-    cluster.sync();   // every CTA's histogram of this pass is complete
-    int sum = 0;
-#pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) sum += *cluster.map_shared_rank(&hist[buf][tid], r);
-    tot[tid] = sum;
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits [8l, 8l+8); find the digit holding the remaining-th
-      // largest key, scanning from the top
-      int c[8], lt = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = tot[8 * lane + i];
-        lt += c[i];
-      }
-      int above = lt;   // inclusive suffix sum over lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, above, o);
-        if (lane + o < 32) above += y;
-      }
-      const int strictly_above = above - lt;
-      const int rem = sh_rem;
-      if (strictly_above < rem && above >= rem) {
-        int acc = strictly_above;
-        int digit = 8 * lane;
-#pragma unroll
-        for (int i = 7; i >= 0; --i) {
-          if (acc + c[i] >= rem) {
-            digit = 8 * lane + i;
-            break;
-          }
-          acc += c[i];
-        }
-        sh_prefix = prefix | ((uint32_t)digit << shift);
-        sh_rem = rem - acc;
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = sh_prefix;
-  const int eq_take = sh_rem;   // keys equal to T to take, lowest page index first
-
-  // ---- compaction in ascending page order
-  const int per = (len + blockDim.x - 1) / blockDim.x;
-  const int c0 = min(len, tid * per), c1 = min(len, c0 + per);
-  int gt = 0, eq = 0;
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t k = keys_s[i];
-    gt += k > T;
-    eq += k == T;
-  }
-  int gt_slice, eq_slice;
-  const int gt_before = block_exclusive_scan(gt, scan_buf, gt_slice);
-  const int eq_before = block_exclusive_scan(eq, scan_buf, eq_slice);
-  if (tid == 0) {
-    slice_cnt[0] = gt_slice;
-    slice_cnt[1] = eq_slice;
-  }
-  cluster.sync();   // every slice's counts are published
-  if (tid == 0) {
-    int g = 0, e = 0;
-    for (int r = 0; r < rank; ++r) {
-      const int* rc = cluster.map_shared_rank(slice_cnt, r);
-      g += rc[0];
-      e += rc[1];
-    }
-    sh_before[0] = g;
-    sh_before[1] = e;
-  }
-  __syncthreads();
-  const int eq_lower = sh_before[1];                      // equal keys in lower slices
-  const int taken_lower = min(eq_lower, eq_take);
-  const int take = max(0, min(eq, eq_take - eq_lower - eq_before));
-  const int take_before = max(0, min(eq_before, eq_take - eq_lower));
-  int pos = sh_before[0] + taken_lower + gt_before + take_before;
-  int taken = 0;
-  for (int i = c0; i < c1; ++i) {
-    const uint32_t k = keys_s[i];
-    if (k > T || (k == T && taken < take)) {
-      if (k == T) ++taken;
-      if (pos < kk) sel[pos] = j0 + i;
-      ++pos;
-    }
-  }
-  if (tid == 0 && rank == 0) p.n_selected[unit] = kk;
-  cluster.sync();   // no CTA leaves while another may still read its counts
+  // [slice keys][cand keys][cand pages][cand blocks][selected list]
+  extern __shared__ __align__(16) uint32_t sel_dyn[];
+  const int slice_cap = (p.max_pages + kSelCluster - 1) / kSelCluster;
+  const int stride = sel_cand_stride(p.max_pages, p.budget, select_fixed_bytes(p.max_pages, p.budget));
+  SelScratch sc;
+  sc.keys_s = sel_dyn;
+  sc.bt_slice = nullptr;
+  sc.cand_key = sel_dyn + slice_cap;
+  sc.cand_page = reinterpret_cast<int*>(sc.cand_key + kSelCluster * stride);
+  sc.cand_blk = sc.cand_page + kSelCluster * stride;
+  sc.cand_stride = stride;
+  sc.out_blk = sc.cand_blk + kSelCluster * stride;
+  cluster_select(p, sc);
 }
 
 }  // namespace locks
@@ -695,8 +433,7 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream) {
-  // dynamic shared memory: one slice of keys (checked against the limit on the host)
-  const size_t dyn = (size_t)((p.max_pages + kSelCluster - 1) / kSelCluster) * sizeof(uint32_t);
+  const size_t dyn = select_smem_bytes(p.max_pages, p.budget);
   static size_t attr_bytes = 0;
   if (dyn > attr_bytes) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);

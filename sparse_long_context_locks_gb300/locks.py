@@ -58,6 +58,10 @@ _SIGS = {
                                    _F, _P, _P, _SZ, _P]),
     "locks_dense_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _I32, _F, _P, _P, _SZ,
                                   _P]),
+    "locks_select_sparse_decode": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _P, _P,
+                                          _P, _F, _P, _P, _SZ, _P]),
+    "locks_decode_step": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _F, _P, _P,
+                                 _P, _P, _P, _SZ, _P]),
     "locks_status_str": (ctypes.c_char_p, [_I32]),
     "locks_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32,
                                            _I32, _F, _P, _P]),
@@ -181,6 +185,31 @@ def locks_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens
         _ptr(block_table), _ptr(seq_lens), _ptr(selected), _ptr(n_selected),
         block_table.shape[0], block_table.shape[1], budget_pages, scale, _ptr(out),
         _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_sparse_decode")
+
+
+def locks_select_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens,
+                               budget_pages, selected, n_selected, out, workspace, scores=None,
+                               sm_scale=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_select_sparse_decode(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_table), _ptr(seq_lens), block_table.shape[0], block_table.shape[1],
+        budget_pages, _ptr(scores), _ptr(selected), _ptr(n_selected), scale, _ptr(out),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_select_sparse_decode")
+
+
+def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table, seq_lens,
+                      budget_pages, selected, n_selected, out, workspace, scores=None,
+                      sm_scale=None, stream=None):
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_decode_step(
+        ctypes.byref(cfg), _ptr(q), _ptr(summaries), _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], _ptr(block_table), _ptr(seq_lens), block_table.shape[0],
+        block_table.shape[1], budget_pages, scale, _ptr(scores), _ptr(selected),
+        _ptr(n_selected), _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_decode_step")
 
 
 def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, out, workspace,

@@ -33,7 +33,7 @@ CODE_EDGE = 0.02
 class Run:
     """One decode step of a workload on the GPU, with every intermediate kept."""
 
-    def __init__(self, w: W.Workload, tail_fill="zero", build=True, dense=False, data=None):
+    def __init__(self, w: W.Workload, tail_fill="zero", build=True, dense=False, data=None, fused=False):
         self.w = w
         self.d = data if data is not None else W.generate(w, device="cuda", tail_fill=tail_fill)
         d = self.d
@@ -55,6 +55,15 @@ class Run:
             self.dense_out = torch.empty_like(self.bufs.out)
             L.locks_dense_decode(H, d["q"], d["k_cache"], d["v_cache"], d["block_table"],
                                  d["seq_lens"], self.dense_out, self.bufs.workspace)
+        self.fused = None
+        if fused:
+            f = {"selected": torch.full_like(self.bufs.selected, -1),
+                 "n_selected": torch.full_like(self.bufs.n_selected, -1),
+                 "out": torch.full_like(self.bufs.out, float("nan"))}
+            L.locks_decode_step(H, d["q"], self.summ, d["k_cache"], d["v_cache"], d["block_table"],
+                                d["seq_lens"], w.budget_pages, f["selected"], f["n_selected"],
+                                f["out"], self.bufs.workspace)
+            self.fused = f
         torch.cuda.synchronize()
         self.status = L.locks_read_status(self.bufs.workspace)
         self.lens = d["seq_lens"].cpu().tolist()
@@ -212,3 +221,20 @@ def check_records(gpu_rec: np.ndarray, K_pages: np.ndarray) -> dict:
     xn = np.linalg.norm((K_pages - summ["mu"][:, None, :]).reshape(P, -1), axis=1)
     assert np.all(eg <= 1.05 * eo + 1e-3 * xn + 1e-6), f"reconstruction worse: {np.max(eg - eo)}"
     return {"pages": P, "well_conditioned": n_well}
+
+
+def check_fused_unit(run: Run, b: int, h: int):
+    """The fused select + attend pass selects exactly what locks_select does
+    (same scores, same selection) and its output matches the oracle's
+    attention over that selection."""
+    f = run.fused
+    ns = int(f["n_selected"][b, h])
+    sel_f = f["selected"][b, h, :ns].cpu().numpy().astype(np.int64)
+    assert sel_f.tolist() == run.gpu_selected(b, h).tolist()
+    L_b = run.lens[b]
+    qg = run.q_group(b, h)
+    kc, vc, bt_row = run.unit_cache(b, h, sel_f)
+    ref = O.sparse_attend_unit(qg, kc, vc, bt_row, 0, L_b, sel_f, 1 / math.sqrt(128))
+    G = run.w.group
+    out = f["out"][b, h * G:(h + 1) * G].double().cpu().numpy()
+    return check_attention(out, ref)

@@ -1,0 +1,83 @@
+"""The fused decode step (locks_decode_step = locks_score followed by the
+cluster kernel of locks_select_sparse_decode) against the separate calls and
+the fp64 oracle, on small edge cases and on the named workloads."""
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_long_context_locks_gb300 import locks as L
+from sparse_long_context_locks_gb300 import workload as W
+
+from gpu_helpers import Run, check_fused_unit, check_unit
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(**kw):
+    base = dict(name="t", batch=1, context=16 * 300 + 7, num_kv_heads=8, group=4,
+                budget_tokens=16 * 24, carriers_per_head=4, seed=11)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+@pytest.mark.parametrize("ctx,heads,budget", [
+    (16 * 300 + 7, 8, 24), (16 * 150 - 1, 2, 24), (16 * 150, 1, 24),     # tail 7 / 15 / 0
+    (16 * 10 + 2, 8, 24), (5, 8, 24), (15, 4, 24),                         # n <= budget, tiny
+    (16 * 2000 + 3, 8, 128), (16 * 64 + 9, 8, 100),                        # many pages / all
+    (16 * 3000 + 1, 4, 1000),                                              # > 8 items per warp
+])
+def test_fused_matches_separate_and_oracle(ctx, heads, budget):
+    w = _w(context=ctx, num_kv_heads=heads, budget_tokens=16 * budget, seed=ctx % 97 + heads)
+    run = Run(w, tail_fill="nan", fused=True)
+    assert run.status == 0
+    for h in range(heads):
+        check_unit(run, 0, h, check_scores_too=False)
+        check_fused_unit(run, 0, h)
+
+
+def test_fused_ragged_batch_and_ties():
+    w = _w(batch=4, context=16 * 90, context_hi=16 * 700, budget_tokens=16 * 40, seed=5)
+    run = Run(w, tail_fill="huge", fused=True)
+    assert run.status == 0
+    for b in range(4):
+        for h in (0, 7):
+            check_fused_unit(run, b, h)
+
+
+def test_fused_step_in_a_graph_is_stable():
+    w = _w(context=16 * 800 + 5, seed=9)
+    run = Run(w, fused=True)
+    first = run.fused["out"].clone()
+    d, H, bufs, f = run.d, run.H, run.bufs, run.fused
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.locks_decode_step(H, d["q"], run.summ, d["k_cache"], d["v_cache"], d["block_table"],
+                            d["seq_lens"], w.budget_pages, f["selected"], f["n_selected"], f["out"],
+                            bufs.workspace)
+    f["out"].zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(first, f["out"])
+    assert L.locks_read_status(bufs.workspace) == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_128k", "ctx1m"])
+def test_fused_named_workloads(name):
+    run = Run(W.CONFIGS[name], fused=True)
+    assert run.status == 0
+    for h in range(8):
+        check_fused_unit(run, 0, h)
+
+
+def test_fused_rejects_unsupported_budget():
+    w = _w(context=16 * 100, budget_tokens=16 * 2048)
+    d = W.generate(w, device="cuda")
+    bufs = L.DecodeBuffers(8, 1, w.max_pages, w.budget_pages)
+    summ = torch.zeros(d["num_blocks"], 8, 784, dtype=torch.uint8, device="cuda")
+    with pytest.raises(L.LocksError) as e:
+        L.locks_select_sparse_decode(8, d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                     d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected,
+                                     bufs.out, bufs.workspace)
+    assert e.value.status == 2
