@@ -11,9 +11,9 @@
 // One cluster of kSelCluster CTAs per (request, KV head).  CTA r owns pages
 // [n r / C, n (r + 1) / C).  Every CTA combines the scoring pass's partial
 // log-sum-exps into Z_g and forms its slice's keys (the fp32 bits of the
-// table entry; non-negative floats order like unsigned ints).  One pass of an
-// 11-bit histogram (exponent and 3 mantissa bits) gives the bin holding the
-// slice's k-th largest key; every key in or above that bin -- a superset of
+// table entry; non-negative floats order like unsigned ints).  One pass of a
+// 1024-bin order-preserving histogram (exponent and 4 mantissa bits) gives the
+// bin holding the slice's k-th largest key; every key in or above that bin -- a superset of
 // the slice's top k -- goes to rank 0's shared memory through distributed
 // shared memory (a crowded bin falls back to an exact radix select).  The
 // global top k is inside the union of those sets, so after one cluster
