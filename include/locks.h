@@ -146,8 +146,7 @@ locks_status locks_build_summaries(const locks_cfg *cfg, const void *k_cache, in
  * for every request b, KV head h and full page j < n_b, read the page's
  * record (and nothing else of the cache) and write, for each query head g of
  * the group, s_j = log sum_i exp((q.mu_j + (V_j^T q).c_i) / sqrt(d)) into
- * `scores` (or into the workspace when scores is NULL), plus per-chunk
- * partial log-sum-exps that locks_select combines. */
+ * `scores` (or into the workspace when scores is NULL). */
 locks_status locks_score(const locks_cfg *cfg, const void *q, const void *summaries,
                          int64_t num_blocks, const int32_t *block_table, const int32_t *seq_lens,
                          int32_t batch, int32_t max_pages, float *scores,
@@ -158,7 +157,10 @@ locks_status locks_score(const locks_cfg *cfg, const void *q, const void *summar
  * exp(s_j - Z); the group's table is the mean share over its G query heads;
  * the min(budget_pages, n_b) largest entries (lower page index on ties) are
  * written to selected[b][h][...] in ascending page order and their count to
- * n_selected[b][h].  `scores` must be what locks_score was given. */
+ * n_selected[b][h].  `scores` must be what locks_score was given.  One
+ * cluster of 8 CTAs per (b, h) computes Z from the scores and selects by an
+ * exact cluster-wide radix select.  Needs max_pages <= 131072, else
+ * LOCKS_ERR_UNSUPPORTED. */
 locks_status locks_select(const locks_cfg *cfg, const int32_t *seq_lens, int32_t batch,
                           int32_t max_pages, int32_t budget_pages, const float *scores,
                           int32_t *selected, int32_t *n_selected,

@@ -27,12 +27,12 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   // scoring
-  int h_cta, wph, pps, head_groups, ch_pages, n_chunks, n_items, score_grid, seg_slots;
+  int h_cta, wph, pps, head_groups, ch_pages, n_chunks, n_items, score_grid;
   // selection
   // attention
   int sparse_splits, sparse_ips, dense_splits, dense_ips, max_splits;
   // workspace regions
-  size_t off_partials, off_scores, off_attn, off_tickets, total;
+  size_t off_scores, off_attn, off_tickets, total;
 };
 
 bool cfg_supported(const locks_cfg* c) {
@@ -66,8 +66,6 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   const int64_t items = (int64_t)batch * pl.head_groups * pl.n_chunks;
   pl.n_items = (int)items;
   pl.score_grid = (int)(items < kTargetCtas ? items : kTargetCtas);
-  // most scoring CTAs one (request, head group) unit's items can span
-  pl.seg_slots = (int)(((int64_t)pl.n_chunks * pl.score_grid + items - 1) / items + 2);
   const int units = batch * H;
   pl.sparse_splits = pick_splits(units, budget + 1);
   pl.sparse_ips = ceil_div(budget + 1, pl.sparse_splits);
@@ -80,8 +78,6 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   size_t off = kAlign;  // [0, 256): status word
   pl.off_tickets = off;
   off = align_up(off + (size_t)units * sizeof(uint32_t));
-  pl.off_partials = off;
-  off = align_up(off + (size_t)batch * pl.head_groups * pl.seg_slots * 8 * kGroup * 2 * sizeof(float));
   pl.off_scores = off;
   off = align_up(off + (size_t)batch * H * max_pages * kGroup * sizeof(float));
   pl.off_attn = off;   // last: its size depends on the split counts
@@ -266,7 +262,6 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.scores = scores ? scores : reinterpret_cast<float*>(ws + pl.off_scores);
-  p.partials = reinterpret_cast<float*>(ws + pl.off_partials);
   p.status = status_word(workspace);
   p.num_blocks = num_blocks;
   p.batch = batch;
@@ -279,7 +274,6 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   p.n_chunks = pl.n_chunks;
   p.head_groups = pl.head_groups;
   p.n_items = pl.n_items;
-  p.seg_slots = pl.seg_slots;
   return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -293,7 +287,6 @@ void fill_select(SelectParams& p, const Plan& pl, const locks_cfg* cfg, const in
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.seq_lens = seq_lens;
   p.scores = scores ? scores : reinterpret_cast<const float*>(ws + pl.off_scores);
-  p.partials = reinterpret_cast<const float*>(ws + pl.off_partials);
   p.selected = selected;
   p.n_selected = n_selected;
   p.status = status_word(workspace);
@@ -301,13 +294,6 @@ void fill_select(SelectParams& p, const Plan& pl, const locks_cfg* cfg, const in
   p.max_pages = max_pages;
   p.H_kv = cfg->num_kv_heads;
   p.budget = budget_pages;
-  p.score_grid = pl.score_grid;
-  p.seg_slots = pl.seg_slots;
-  p.n_items = pl.n_items;
-  p.n_chunks = pl.n_chunks;
-  p.head_groups = pl.head_groups;
-  p.h_cta = pl.h_cta;
-  p.wph = pl.wph;
 }
 
 }  // namespace
@@ -326,7 +312,9 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   LOCKS_CHECK_PTR(workspace);
   if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
   if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
-  if (select_smem_bytes(max_pages, budget_pages) > (size_t)kSmemLimit) return LOCKS_ERR_UNSUPPORTED;
+  if ((max_pages + kSelCluster - 1) / kSelCluster > kFusedMaxKeysPerCta ||
+      select_smem_bytes(max_pages, budget_pages) > (size_t)kSmemLimit)
+    return LOCKS_ERR_UNSUPPORTED;
   const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
   if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
   SelectParams p{};

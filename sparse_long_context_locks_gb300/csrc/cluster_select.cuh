@@ -5,22 +5,33 @@
 // "LOCKS: Page-Local Compact Key Summaries for Efficient Long-Context
 // Decoding", technical summary §2, "Reconstruction and selection" and
 // "Group-shared selection (GQA)": per-head page-mass shares exp(s_j - Z_g),
-// averaged over the group's query heads into one table; the k largest entries
-// (lower page index on ties) are attended.
+// Z_g = log sum_j exp(s_j,g) over the full pages, averaged over the group's
+// query heads into one table; the k largest entries (lower page index on
+// ties) are attended.
 //
-// One cluster of kSelCluster CTAs per (request, KV head).  CTA r owns pages
-// [n r / C, n (r + 1) / C).  Every CTA combines the scoring pass's partial
-// log-sum-exps into Z_g and forms its slice's keys (the fp32 bits of the
-// table entry; non-negative floats order like unsigned ints).  One pass of a
-// 1024-bin order-preserving histogram (exponent and 4 mantissa bits) gives the
-// bin holding the slice's k-th largest key; every key in or above that bin -- a superset of
-// the slice's top k -- goes to rank 0's shared memory through distributed
-// shared memory (a crowded bin falls back to an exact radix select).  The
-// global top k is inside the union of those sets, so after one cluster
-// barrier rank 0 finds the boundary bin of the candidates the same way,
-// ranks the few candidates inside it exactly (key, then lower page), and
-// writes the result in ascending page order; after a second barrier every CTA
-// may read it.
+// One cluster of kSelCluster CTAs per (request, KV head); CTA r owns pages
+// [n r / C, n (r + 1) / C).
+//   1. Z_g: each CTA folds its slice's scores into a (max, sum) pair per head
+//      and publishes it in shared memory; after a cluster barrier every CTA
+//      combines the C pairs, read through distributed shared memory.
+//   2. Keys: the fp32 bits of the table entries (non-negative floats order
+//      like unsigned ints).
+//   3. Exact cluster-wide select.  Level 0: every CTA histograms its keys by
+//      bits 30-20 (exponent and 3 mantissa bits) and publishes its highest
+//      occupied bin; after a cluster barrier every CTA walks the C
+//      histograms top-down from the highest bin, 32 bins (one remote count
+//      per thread) at a time, to the bin holding the k-th largest key, and
+//      takes from the per-CTA counts above it its own number of selected keys
+//      and the number selected by lower-ranked CTAs (its output offset).  The
+//      boundary bin's members (typically tens to a few hundred) then go to
+//      rank 0 as (key, page), and every CTA ranks all of them exactly (key
+//      descending, lower page first), a thread per member.  When the bin holds more
+//      than kMemberCap keys, levels over bits 19-10 and 9-0 follow instead,
+//      each a full histogram exchange; after the last one the boundary keys
+//      are equal and the lowest pages go first.
+//   4. Each CTA writes its selected pages, ascending, from its offset on, and
+//      their physical blocks into rank 0's shared memory; a final cluster
+//      barrier publishes that list.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -33,9 +44,12 @@ namespace locks {
 namespace cg = cooperative_groups;
 
 constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelMaxChunks = kFusedMaxKeysPerCta / 32;   // 32-key chunks of one slice
+constexpr int kMemberCap = 512;   // boundary-bin members ranked pairwise after level 0
 
-// Merge of two (max, sum) log-sum-exp partials (natural-log units).
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+// Merge of two (max, sum) log-sum-exp partials (log2 units).
+__device__ __forceinline__ void lse2_merge(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
     m = m2;
@@ -43,10 +57,10 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     return;
   }
   if (m2 > m) {
-    s = s * fast_exp2((m - m2) * kLog2e) + s2;
+    s = s * fast_exp2(m - m2) + s2;
     m = m2;
   } else {
-    s += s2 * fast_exp2((m2 - m) * kLog2e);
+    s += s2 * fast_exp2(m2 - m);
   }
 }
 
@@ -77,157 +91,33 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_buf, int& t
   return before;
 }
 
-// Warp-aggregated shared-memory histogram add: lanes holding the same bin add once.
-__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool active) {
-  const uint32_t act = __ballot_sync(0xffffffffu, active);
-  if (active) {
-    const uint32_t peers = __match_any_sync(act, bin);
-    if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[bin], (int)__popc(peers));
+// Block-wide sums of two ints (every thread gets both); ends with a barrier.
+__device__ __forceinline__ void block_sum2(int& a, int& b, int* warp_buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
   }
-}
-
-// Selection rule produced by block_radix_select: a key k is selected when
-// (k >> shift) > prefix, or when (k >> shift) == prefix and it is among the
-// first `take` such keys in index order.
-struct RadixCut {
-  uint32_t prefix;
-  int shift;
-  int take;
-};
-
-// Block-wide radix select (8-bit digits, MSB first) of the `need`-th largest
-// of keys[0, cnt) in shared memory; stops early once the boundary bin holds
-// exactly the keys still needed.  Every thread of the block must call it.
-static __device__ RadixCut block_radix_select(const uint32_t* keys, int cnt, int need) {
-  __shared__ int hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_rem, s_shift, s_done;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    s_prefix = 0;
-    s_rem = need;
-    s_shift = 0;
-    s_done = 0;
-  }
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = s_prefix;
-    const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int base = tid & ~31; base < cnt; base += blockDim.x) {
-      const int i = base + lane;
-      uint32_t k = 0;
-      bool match = false;
-      if (i < cnt) {
-        k = keys[i];
-        match = (k & hmask) == (prefix & hmask);
-      }
-      hist_add(hist, (k >> shift) & 255u, match);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits [8l, 8l+8); find the digit holding the rem-th
-      // largest key, scanning from the top
-      int c[8], lt = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = hist[8 * lane + i];
-        lt += c[i];
-      }
-      int above = lt;   // inclusive suffix sum over lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, above, o);
-        if (lane + o < 32) above += y;
-      }
-      const int strictly_above = above - lt;
-      const int rem = s_rem;
-      if (strictly_above < rem && above >= rem) {
-        int acc = strictly_above;
-        int digit = 8 * lane, dcount = 0;
-#pragma unroll
-        for (int i = 7; i >= 0; --i) {
-          if (acc + c[i] >= rem) {
-            digit = 8 * lane + i;
-            dcount = c[i];
-            break;
-          }
-          acc += c[i];
-        }
-        s_prefix = prefix | ((uint32_t)digit << shift);
-        s_rem = rem - acc;
-        s_shift = shift;
-        if (rem - acc == dcount) s_done = 1;   // every key left in the bin is needed
-      }
-    }
-    __syncthreads();
-    if (s_done) break;
-  }
-  RadixCut cut{s_prefix >> s_shift, s_shift, s_rem};
-  __syncthreads();
-  return cut;
-}
-
-// Histogram bin of a key: order-preserving (a larger key never falls in a
-// lower bin).  Table entries lie in [0, 1]; exponents 64..127 get 16 bins
-// each (4 mantissa bits, 6.25 % wide), everything below 2^-63 shares bin 0.
-constexpr int kBins = 1024;
-constexpr int kExactCap = 256;     // boundary-bin members ranked pairwise
-static_assert(3 * kExactCap <= kBins, "bin members reuse the histogram");
-__device__ __forceinline__ int key_bin(uint32_t key) {
-  const int b = (int)(key >> 19) - 1024;
-  return b < 0 ? 0 : (b > kBins - 1 ? kBins - 1 : b);
-}
-
-// Block-wide histogram of key_bin over keys[0, cnt) and the bin holding the
-// need-th largest key (1 <= need <= cnt).  Every thread must call it.
-struct BinCut {
-  int bin;
-  int above;   // keys in higher bins
-  int count;   // keys in the bin
-};
-static __device__ BinCut block_bin_cut(const uint32_t* keys, int cnt, int need, int* hist, int* scan_buf) {
-  __shared__ BinCut s_cut;
-  const int tid = threadIdx.x;
-  constexpr int kPer = kBins / kSelThreads;
-  for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  for (int i = tid; i < cnt; i += blockDim.x) atomicAdd(&hist[key_bin(keys[i])], 1);
-  __syncthreads();
-  // thread t owns bins top, top - 1, ..., top - kPer + 1, scanned from the top
-  const int top = kBins - 1 - kPer * tid;
-  int c[kPer], tot = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    c[i] = hist[top - i];
-    tot += c[i];
-  }
-  int all;
-  const int above = block_exclusive_scan(tot, scan_buf, all);
-  if (above < need && above + tot >= need) {
-    int acc = above;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      if (acc + c[i] >= need) {
-        s_cut = BinCut{top - i, acc, c[i]};
-        break;
-      }
-      acc += c[i];
-    }
+  if (lane == 0) {
+    warp_buf[2 * warp] = a;
+    warp_buf[2 * warp + 1] = b;
   }
   __syncthreads();
-  const BinCut cut = s_cut;
+  a = 0;
+  b = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    a += warp_buf[2 * w];
+    b += warp_buf[2 * w + 1];
+  }
   __syncthreads();
-  return cut;
 }
 
-// First item of CTA c of the scoring grid, and the CTA holding item x.
-__host__ __device__ __forceinline__ long long score_item_begin(long long c, long long n_items, long long grid) {
-  return (c * n_items) / grid;
-}
-__host__ __device__ __forceinline__ int score_cta_of(long long x, long long n_items, long long grid) {
-  return (int)(((x + 1) * grid - 1) / n_items);
+// Radix levels over the 31 value bits of a non-negative float's pattern.
+__device__ __forceinline__ int lvl_shift(int lvl) { return lvl == 0 ? 20 : (lvl == 1 ? 10 : 0); }
+__device__ __forceinline__ int lvl_bits(int lvl) { return lvl == 0 ? 11 : 10; }
+__device__ __forceinline__ uint32_t lvl_digit(uint32_t key, int lvl) {
+  return (key >> lvl_shift(lvl)) & ((1u << lvl_bits(lvl)) - 1u);
 }
 
 // Result of cluster_select for the calling CTA.
@@ -237,20 +127,14 @@ struct ClusterSel {
   int kk;       // pages selected for the unit
 };
 
-// Scratch layout (shared memory) handed to cluster_select:
-//   keys_s   ceil(max_pages / C) words: this CTA's keys;
+// Shared-memory scratch handed to cluster_select:
+//   keys_s   ceil(max_pages / C) <= kFusedMaxKeysPerCta words: this CTA's keys;
 //   bt_slice optional block ids of this CTA's pages (nullptr: none);
-//   cand_*   C * min(budget, ceil(max_pages / C)) entries each, used on rank 0:
-//            the local winners of every CTA, then rank 0's selection;
-//   out_blk  rank 0: the selected pages' physical blocks (bt_slice given) or
-//            page indices, ascending by page.
+//   out_blk  budget words, used on rank 0: the selected pages' physical
+//            blocks (bt_slice given) or page indices, ascending by page.
 struct SelScratch {
   uint32_t* keys_s;
   const int* bt_slice;
-  uint32_t* cand_key;
-  int* cand_page;
-  int* cand_blk;
-  int cand_stride;      // entries per CTA in the cand arrays
   int* out_blk;
 };
 
@@ -259,17 +143,22 @@ struct SelScratch {
 // a cluster barrier after which rank 0's out_blk[0, kk) may be read through
 // distributed shared memory.
 static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScratch& sc) {
-  __shared__ float red[kSelThreads / 32][kGroup], red2[kSelThreads / 32][kGroup];
-  __shared__ int hist_s[kBins];
+  __shared__ __align__(16) int hist0[1 << 11];
+  __shared__ __align__(16) int hist1[1 << 10];
+  __shared__ __align__(16) int hist2[1 << 10];
+  __shared__ int s_hmax;                       // this CTA's highest occupied level-0 bin
+  __shared__ __align__(8) float lse_pub[kGroup][2];   // this CTA's (max, sum) per head, log2 units
+  __shared__ float red_m[kSelWarps][kGroup], red_s[kSelWarps][kGroup];
   __shared__ float zl[kGroup];
   __shared__ int scan_buf[32];
-  __shared__ int cand_count[kSelCluster];
-  __shared__ int s_ncover;
+  __shared__ int bnd_cnt[kSelCluster];         // per-CTA count in the boundary bin
+  __shared__ int s_bin, s_above, s_bt_mine, s_bt_before, s_cutoff, s_cnt;
+  __shared__ int chunk_base[kSelMaxChunks];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int unit = blockIdx.y;              // (request, KV head)
-  const int b = unit / p.H_kv, h = unit % p.H_kv;
+  const int b = unit / p.H_kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int L = p.seq_lens[b];
   int32_t* sel = p.selected + (int64_t)unit * p.budget;
@@ -278,7 +167,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   if (L < 0 || (L + kPage - 1) / kPage > p.max_pages) {
     if (tid == 0 && rank == 0) {
       p.n_selected[unit] = 0;
-      if (h == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
+      if (unit % p.H_kv == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
     }
     cluster.sync();
     return res;
@@ -291,281 +180,396 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   const int j0 = (int)(((long long)n * rank) / kSelCluster);
   const int j1 = (int)(((long long)n * (rank + 1)) / kSelCluster);
   const int len = j1 - j0;
-  if (n <= p.budget) {   // every full page is selected
-    for (int i = tid; i < len; i += blockDim.x) {
-      sel[j0 + i] = j0 + i;
-      // rank 0 holds the list: fill its out_blk through distributed shared memory
-      *cluster.map_shared_rank(&sc.out_blk[j0 + i], 0) = sc.bt_slice ? sc.bt_slice[i] : j0 + i;
+  if (n <= p.budget || kk == 0) {   // every full page is selected (or none is)
+    if (kk > 0) {
+      for (int i = tid; i < len; i += blockDim.x) {
+        sel[j0 + i] = j0 + i;
+        // rank 0 holds the list: fill its out_blk through distributed shared memory
+        *cluster.map_shared_rank(&sc.out_blk[j0 + i], 0) = sc.bt_slice ? sc.bt_slice[i] : j0 + i;
+      }
     }
-    if (tid == 0 && rank == 0) p.n_selected[unit] = n;
+    if (tid == 0 && rank == 0) p.n_selected[unit] = kk;
     cluster.sync();
     return res;
   }
 
-  // ---- this thread's first scores, issued before the partials' loads
-  const float4* srow = reinterpret_cast<const float4*>(p.scores + (int64_t)unit * p.max_pages * kGroup);
-  constexpr int kPre = 4;
+  // ---- 1. this slice's (max, sum) of the scores per head, log2 units
+  const float4* srow = reinterpret_cast<const float4*>(p.scores + (int64_t)unit * p.max_pages * kGroup) + j0;
+  constexpr int kPre = 4;   // scores held in registers for both passes
   float4 pre[kPre];
 #pragma unroll
   for (int r = 0; r < kPre; ++r) {
     const int i = tid + r * kSelThreads;
-    pre[r] = i < len ? srow[j0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    pre[r] = i < len ? srow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-
-  // ---- Z_g from the scoring pass's partials: slots (unit u, covering CTA)
-  const int hg = h / p.h_cta, hl = h % p.h_cta;
-  const long long u = (long long)b * p.head_groups + hg;
-  if (tid == 0) {
-    const int cf = score_cta_of(u * p.n_chunks, p.n_items, p.score_grid);
-    const int cl = score_cta_of(u * p.n_chunks + p.n_chunks - 1, p.n_items, p.score_grid);
-    s_ncover = cl - cf + 1;
+  for (int i = tid; i < (1 << 10); i += blockDim.x) {
+    hist1[i] = 0;
+    hist2[i] = 0;
   }
-  __syncthreads();
-  const int nent = s_ncover * p.wph;
+  for (int i = tid; i < (1 << 11); i += blockDim.x) hist0[i] = 0;
+  if (tid == 0) s_hmax = -1;
   {
-    // each warp folds entries warp, warp + 8, ... (lane-strided), then the
-    // block merges the 8 warps' (max, sum) per head
     float m[kGroup] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    float sm[kGroup] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = tid; i < nent; i += blockDim.x) {
-      const int slot = i / p.wph, sub = i % p.wph;
-      const float4* part = reinterpret_cast<const float4*>(
-          p.partials + ((((int64_t)u * p.seg_slots + slot) * 8 + hl * p.wph + sub) * kGroup * 2));
-      const float4 a = part[0], c = part[1];   // (m0 s0 m1 s1) (m2 s2 m3 s3)
-      lse_merge(m[0], sm[0], a.x, a.y);
-      lse_merge(m[1], sm[1], a.z, a.w);
-      lse_merge(m[2], sm[2], c.x, c.y);
-      lse_merge(m[3], sm[3], c.z, c.w);
-    }
+    float s[kGroup] = {0.f, 0.f, 0.f, 0.f};
+    auto fold = [&](const float4& v) {
+      const float x[kGroup] = {v.x * kLog2e, v.y * kLog2e, v.z * kLog2e, v.w * kLog2e};
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const float mn = fmaxf(m[g], x[g]);
+        s[g] = s[g] * fast_exp2(m[g] - mn) + fast_exp2(x[g] - mn);
+        m[g] = mn;
+      }
+    };
+#pragma unroll
+    for (int r = 0; r < kPre; ++r)
+      if (tid + r * kSelThreads < len) fold(pre[r]);
+#pragma unroll 4
+    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) fold(srow[i]);
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       float mx = m[g];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float sv = m[g] == -INFINITY ? 0.f : sm[g] * fast_exp2((m[g] - mx) * kLog2e);
+      float sv = m[g] == -INFINITY ? 0.f : s[g] * fast_exp2(m[g] - mx);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
       if (lane == 0) {
-        red[warp][g] = mx;
-        red2[warp][g] = sv;
+        red_m[warp][g] = mx;
+        red_s[warp][g] = sv;
       }
     }
     __syncthreads();
     if (tid < kGroup) {
       float mx = -INFINITY, sv = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSelThreads / 32; ++w) lse_merge(mx, sv, red[w][tid], red2[w][tid]);
-      zl[tid] = (mx + logf(sv)) * kLog2e;   // log2 units
+      for (int w = 0; w < kSelWarps; ++w) lse2_merge(mx, sv, red_m[w][tid], red_s[w][tid]);
+      lse_pub[tid][0] = mx;
+      lse_pub[tid][1] = sv;
     }
-    __syncthreads();
   }
+  cluster.sync();   // every CTA's (max, sum) pairs and cleared histograms are visible
+  if (tid < kGroup) {
+    float2 pr[kSelCluster];   // issue every remote load before merging
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r)
+      pr[r] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(&lse_pub[tid][0], r));
+    float mx = -INFINITY, sv = 0.f;
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) lse2_merge(mx, sv, pr[r].x, pr[r].y);
+    zl[tid] = mx + fast_log2(sv);   // log2 Z_g
+  }
+  __syncthreads();
 
-  // ---- keys of this slice
+  // ---- 2. keys of this slice: mean over heads of exp(s - Z_g), as fp32 bits
   {
     const float z0 = zl[0], z1 = zl[1], z2 = zl[2], z3 = zl[3];
-    auto key_of = [&](float4 sv) {
-      float avg = 0.25f * (fast_exp2(sv.x * kLog2e - z0) + fast_exp2(sv.y * kLog2e - z1) +
-                           fast_exp2(sv.z * kLog2e - z2) + fast_exp2(sv.w * kLog2e - z3));
+    uint32_t kmax = 0u;
+    bool any = false;
+    auto make_key = [&](const float4& v, int i) {
+      float avg = 0.25f * (fast_exp2(v.x * kLog2e - z0) + fast_exp2(v.y * kLog2e - z1) +
+                           fast_exp2(v.z * kLog2e - z2) + fast_exp2(v.w * kLog2e - z3));
       if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
-      return __float_as_uint(avg);
+      const uint32_t key = __float_as_uint(avg);
+      sc.keys_s[i] = key;
+      atomicAdd(&hist0[lvl_digit(key, 0)], 1);
+      kmax = max(kmax, key);
+      any = true;
     };
 #pragma unroll
     for (int r = 0; r < kPre; ++r) {
       const int i = tid + r * kSelThreads;
-      if (i < len) sc.keys_s[i] = key_of(pre[r]);
+      if (i < len) make_key(pre[r], i);
     }
 #pragma unroll 4
-    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) sc.keys_s[i] = key_of(srow[j0 + i]);
+    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) make_key(srow[i], i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    if (__any_sync(0xffffffffu, any) && lane == 0) atomicMax(&s_hmax, (int)lvl_digit(kmax, 0));
   }
-  __syncthreads();
 
-  // ---- this slice's candidates (a superset of its top kk), to rank 0 in
-  // ascending page order
+  // ---- 3. cluster-wide select
+  uint32_t bnd[3] = {0u, 0u, 0u};
+  int need = kk;        // keys still to take among those in play
+  int mine = 0;         // keys this CTA selects above the boundary so far
+  int before = 0;       // keys lower-ranked CTAs select above the boundary so far
+  int final_lvl = 2;    // -1: boundary members marked by bit 31 of their key
+  cluster.sync();       // level-0 histograms and highest bins are complete
+
+  // level 0: walk the bins top-down from the highest occupied one, 32 bins a
+  // round; thread t reads CTA (t % 8)'s count of bin top - t / 8
   {
-    const int lk = min(kk, len);
-    // selection rule for this slice: key >> shift > prefix, or == prefix and
-    // among the first `take` (index order)
-    // (bin rule: every key whose bin is at or above the cut bin)
-    RadixCut cut{0u, 31, len};   // len <= kk: every key (bit 31 is clear)
-    int min_bin = 0;
-    bool by_bin = true;
-    if (len > kk) {
-      const BinCut bc = block_bin_cut(sc.keys_s, len, lk, hist_s, scan_buf);
-      if (bc.above + bc.count <= sc.cand_stride) {
-        min_bin = bc.bin;
-      } else {
-        by_bin = false;
-        cut = block_radix_select(sc.keys_s, len, lk);   // crowded bin: exact local top lk
-      }
-    }
-    const int per = (len + blockDim.x - 1) / blockDim.x;
-    const int c0 = min(len, tid * per), c1 = min(len, c0 + per);
-    int gt = 0, eq = 0;
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t key = sc.keys_s[i];
-      if (by_bin) {
-        gt += key_bin(key) >= min_bin;
-      } else {
-        const uint32_t k = key >> cut.shift;
-        gt += k > cut.prefix;
-        eq += k == cut.prefix;
-      }
-    }
-    int gt_tot, eq_tot;
-    const int gt_before = block_exclusive_scan(gt, scan_buf, gt_tot);
-    const int eq_before = block_exclusive_scan(eq, scan_buf, eq_tot);
-    const int take = max(0, min(eq, cut.take - eq_before));
-    int pos = gt_before + max(0, min(eq_before, cut.take));
-    int taken = 0;
-    uint32_t* rkey = cluster.map_shared_rank(sc.cand_key, 0) + rank * sc.cand_stride;
-    int* rpage = cluster.map_shared_rank(sc.cand_page, 0) + rank * sc.cand_stride;
-    int* rblk = cluster.map_shared_rank(sc.cand_blk, 0) + rank * sc.cand_stride;
-    for (int i = c0; i < c1; ++i) {
-      const uint32_t key = sc.keys_s[i];
-      const uint32_t k = key >> cut.shift;
-      const bool in_bin = by_bin && key_bin(key) >= min_bin;
-      const bool eqk = !by_bin && k == cut.prefix;
-      if (in_bin || (!by_bin && k > cut.prefix) || (eqk && taken < take)) {
-        if (eqk) ++taken;
-        rkey[pos] = key;
-        rpage[pos] = j0 + i;
-        rblk[pos] = sc.bt_slice ? sc.bt_slice[i] : j0 + i;
-        ++pos;
-      }
-    }
-    if (tid == 0) *cluster.map_shared_rank(&cand_count[rank], 0) = gt_tot + min(eq_tot, cut.take);
-  }
-  cluster.sync();   // every CTA's local winners are on rank 0
-
-  // ---- rank 0: exact top-kk among the candidates, ascending page order
-  if (rank == 0) {
-    // pack the C segments in rank order (rank r's pages precede rank r+1's)
-    __shared__ int seg_base[kSelCluster + 1];
+    if (tid < kSelCluster) scan_buf[tid] = *cluster.map_shared_rank(&s_hmax, tid);
+    __syncthreads();
+    int hi = -1;
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) hi = max(hi, scan_buf[r]);
+    __syncthreads();
+    const int r_of = tid % kSelCluster;
+    int add_mine = 0, add_before = 0;
+    int carry = 0;   // keys in the bins above this round
+    bool found = false;
     if (tid == 0) {
-      int acc = 0;
-      for (int r = 0; r < kSelCluster; ++r) {
-        seg_base[r] = acc;
-        acc += cand_count[r];
+      s_bin = 0;
+      s_above = 0;
+    }
+    for (int top = hi; top >= 0 && !found; top -= kSelThreads / kSelCluster) {
+      const int bin = top - tid / kSelCluster;
+      const int v = bin >= 0 ? *cluster.map_shared_rank(&hist0[bin], r_of) : 0;
+      // bin total over the 8 CTAs: lanes 8k..8k+7 hold one bin
+      int tot = v;
+#pragma unroll
+      for (int o = 1; o < kSelCluster; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      int round_total;
+      const int above = carry + block_exclusive_scan(r_of == 0 ? tot : 0, scan_buf, round_total);
+      // `above` on lane r_of == 0 of each bin; share it with the bin's lanes
+      const int above_bin = __shfl_sync(0xffffffffu, above, lane & ~(kSelCluster - 1));
+      const bool is_bnd = bin >= 0 && above_bin < need && above_bin + tot >= need;
+      if (is_bnd) {
+        bnd_cnt[r_of] = v;
+        if (r_of == 0) {
+          s_bin = bin;
+          s_above = above_bin;
+        }
       }
-      seg_base[kSelCluster] = acc;
+      found = __syncthreads_or(is_bnd);
+      if (!found) {
+        if (r_of == rank) add_mine += v;
+        if (r_of < rank) add_before += v;
+        carry += round_total;
+        continue;
+      }
+      if (bin > s_bin) {
+        if (r_of == rank) add_mine += v;
+        if (r_of < rank) add_before += v;
+      }
+    }
+    if (!found && tid == 0) flag_status(p.status, LOCKS_FLAG_BAD_SELECT);   // counts inconsistent: cannot happen
+    block_sum2(add_mine, add_before, scan_buf);
+    mine += add_mine;
+    before += add_before;
+    bnd[0] = (uint32_t)s_bin;
+    need -= s_above;
+  }
+  int in_bin = 0, lower = 0;
+#pragma unroll
+  for (int r = 0; r < kSelCluster; ++r) {
+    in_bin += bnd_cnt[r];
+    if (r < rank) lower += bnd_cnt[r];
+  }
+  if (in_bin == need) {   // the boundary bin is needed whole
+    final_lvl = 0;
+    before += lower;
+    mine += bnd_cnt[rank];
+    if (tid == 0) s_cutoff = len;
+    __syncthreads();
+  } else if (in_bin <= kMemberCap) {
+    // The boundary bin's members go to rank 0 as (key, page); every CTA then
+    // ranks all of them exactly (key descending, lower page first) and marks
+    // its own taken members with bit 31 of their key (free: the keys are
+    // non-negative floats).  The level-1 and level-2 histograms are unused
+    // on this path: their storage holds the members (rank 0's copy in
+    // hist1, a local copy in hist2).
+    uint32_t* mkey = reinterpret_cast<uint32_t*>(hist1);
+    int* mpage = hist1 + kMemberCap;
+    // local copy as one sortable word per member: key above, ~page below, so
+    // a larger word ranks first (larger key, then lower page)
+    unsigned long long* lword = reinterpret_cast<unsigned long long*>(hist2);
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    uint32_t* rkey = cluster.map_shared_rank(mkey, 0) + lower;
+    int* rpage = cluster.map_shared_rank(mpage, 0) + lower;
+    for (int i = tid; i < len; i += blockDim.x) {
+      const uint32_t key = sc.keys_s[i];
+      if (lvl_digit(key, 0) == bnd[0]) {
+        const int slot = atomicAdd(&s_cnt, 1);
+        rkey[slot] = key;
+        rpage[slot] = j0 + i;
+      }
+    }
+    cluster.sync();   // every CTA's members are on rank 0
+    {
+      const uint32_t* k0 = cluster.map_shared_rank(mkey, 0);
+      const int* p0 = cluster.map_shared_rank(mpage, 0);
+      for (int x = tid; x < in_bin; x += blockDim.x)
+        lword[x] = ((unsigned long long)k0[x] << 32) | (0xFFFFFFFFu - (uint32_t)p0[x]);
     }
     __syncthreads();
-    const int total = seg_base[kSelCluster];
-    // compact in place: segment r moves from [r * stride, ...) down to seg_base[r]
-    // (seg_base[r] <= r * stride, and segments move in rank order, one
-    // segment per pass so no entry is overwritten before it is read)
-    for (int r = 1; r < kSelCluster; ++r) {
-      const int cnt = cand_count[r], from = r * sc.cand_stride, to = seg_base[r];
-      if (to != from) {
-        for (int i0 = 0; i0 < cnt; i0 += blockDim.x) {
-          const int i = i0 + tid;
-          uint32_t k = 0;
-          int pg = 0, bk = 0;
-          if (i < cnt) {
-            k = sc.cand_key[from + i];
-            pg = sc.cand_page[from + i];
-            bk = sc.cand_blk[from + i];
-          }
-          __syncthreads();
-          if (i < cnt) {
-            sc.cand_key[to + i] = k;
-            sc.cand_page[to + i] = pg;
-            sc.cand_blk[to + i] = bk;
-          }
-          __syncthreads();
+    // thread x ranks member x against all members (broadcast reads)
+    int own_taken = 0, lower_taken = 0;
+    for (int x = tid; x < in_bin; x += blockDim.x) {
+      const unsigned long long wx = lword[x];
+      int rk = 0;
+#pragma unroll 8
+      for (int y = 0; y < in_bin; ++y) rk += lword[y] > wx;
+      if (rk < need) {
+        const int px = (int)(0xFFFFFFFFu - (uint32_t)wx);
+        if (px < j0) {
+          ++lower_taken;
+        } else if (px < j1) {
+          ++own_taken;
+          sc.keys_s[px - j0] = (uint32_t)(wx >> 32) | 0x80000000u;
         }
       }
     }
-    // boundary bin of the kk-th largest candidate; its members are ranked
-    // exactly (key descending, then lower page) when few, else a radix
-    // select over all candidates decides
-    __shared__ int bin_n;
-    const BinCut bc = block_bin_cut(sc.cand_key, total, kk, hist_s, scan_buf);
-    // the histogram is free again: it holds the boundary bin's members
-    int* bin_idx = hist_s;
-    uint32_t* bin_key = reinterpret_cast<uint32_t*>(hist_s + kExactCap);
-    int* bin_page = hist_s + 2 * kExactCap;
-    const int need = kk - bc.above;
-    const bool exact_bin = bc.count <= kExactCap;
-    RadixCut fin{0u, 0, 0};
-    if (exact_bin) {
-      if (tid == 0) bin_n = 0;
-      __syncthreads();
-      for (int i = tid; i < total; i += blockDim.x) {
-        const uint32_t key = sc.cand_key[i];
-        if (key_bin(key) == bc.bin) {
-          const int slot = atomicAdd(&bin_n, 1);
-          bin_idx[slot] = i;
-          bin_key[slot] = key;
-          bin_page[slot] = sc.cand_page[i];
-        }
+    block_sum2(own_taken, lower_taken, scan_buf);
+    mine += own_taken;
+    before += lower_taken;
+    final_lvl = -1;
+    if (tid == 0) s_cutoff = len;
+    __syncthreads();
+  } else {
+    // crowded boundary bin: full histogram exchanges over the lower digits
+    for (int lvl = 1; lvl < 3; ++lvl) {
+      int* hist = lvl == 1 ? hist1 : hist2;
+      for (int i = tid; i < len; i += blockDim.x) {
+        const uint32_t key = sc.keys_s[i];
+        if (lvl_digit(key, 0) == bnd[0] && (lvl < 2 || lvl_digit(key, 1) == bnd[1]))
+          atomicAdd(&hist[lvl_digit(key, lvl)], 1);
       }
-      __syncthreads();
-      // a member is taken when fewer than `need` members precede it
-      // (larger key, or equal key and lower page); taken members get bit 31
-      // of their candidate key set (free: the keys are non-negative floats)
-      const int nb = bin_n;
-      for (int a = tid; a < nb; a += blockDim.x) {
-        const uint32_t ka = bin_key[a];
-        const int pa = bin_page[a];
-        int before = 0;
-        for (int bb = 0; bb < nb; ++bb) {
-          const uint32_t kb = bin_key[bb];
-          before += kb > ka || (kb == ka && bin_page[bb] < pa);
-        }
-        if (before < need) sc.cand_key[bin_idx[a]] = ka | 0x80000000u;
+      cluster.sync();   // every CTA's histogram of this level is complete
+      // thread t owns bins [lo_bin, lo_bin + 4), highest first
+      constexpr int per = 4;
+      const int top = (1 << 10) - 1 - per * tid;
+      const int lo_bin = top - per + 1;
+      int v[kSelCluster][per];
+#pragma unroll
+      for (int r = 0; r < kSelCluster; ++r) {   // every remote load first
+        const int4 q = *reinterpret_cast<const int4*>(cluster.map_shared_rank(hist, r) + lo_bin);
+        v[r][0] = q.x;
+        v[r][1] = q.y;
+        v[r][2] = q.z;
+        v[r][3] = q.w;
       }
-      __syncthreads();
-    } else {
-      fin = block_radix_select(sc.cand_key, total, kk);
-    }
-    const int per = (total + blockDim.x - 1) / blockDim.x;
-    const int c0 = min(total, tid * per), c1 = min(total, c0 + per);
-    auto chosen_exact = [&](uint32_t key) {
-      return (key >> 31) != 0u || key_bin(key) > bc.bin;
-    };
-    int pos;
-    if (exact_bin) {
-      int cnt = 0;
-      for (int i = c0; i < c1; ++i) cnt += chosen_exact(sc.cand_key[i]);
-      int all;
-      pos = block_exclusive_scan(cnt, scan_buf, all);
-      for (int i = c0; i < c1; ++i)
-        if (chosen_exact(sc.cand_key[i])) {
-          if (pos < kk) {
-            sel[pos] = sc.cand_page[i];
-            sc.out_blk[pos] = sc.cand_blk[i];
+      int c[per] = {0, 0, 0, 0};
+#pragma unroll
+      for (int r = 0; r < kSelCluster; ++r)
+#pragma unroll
+        for (int i = 0; i < per; ++i) c[i] += v[r][i];
+      const int cnt_all = c[0] + c[1] + c[2] + c[3];
+      int total;
+      const int above = block_exclusive_scan(cnt_all, scan_buf, total);
+      const bool holder = above < need && above + cnt_all >= need;
+      if (holder) {
+        int acc = above, bi = per - 1;
+#pragma unroll
+        for (int i = per - 1; i >= 0; --i) {
+          if (acc + c[i] >= need) {
+            bi = i;
+            break;
           }
-          ++pos;
+          acc += c[i];
         }
-    } else {
-      int gt = 0, eq = 0;
-      for (int i = c0; i < c1; ++i) {
-        const uint32_t k = sc.cand_key[i] >> fin.shift;
-        gt += k > fin.prefix;
-        eq += k == fin.prefix;
+        s_bin = lo_bin + bi;
+        s_above = acc;
       }
-      int gt_tot, eq_tot;
-      const int gt_before = block_exclusive_scan(gt, scan_buf, gt_tot);
-      const int eq_before = block_exclusive_scan(eq, scan_buf, eq_tot);
-      const int take = max(0, min(eq, fin.take - eq_before));
-      pos = gt_before + max(0, min(eq_before, fin.take));
-      int taken = 0;
-      for (int i = c0; i < c1; ++i) {
-        const uint32_t k = sc.cand_key[i] >> fin.shift;
-        if (k > fin.prefix || (k == fin.prefix && taken < take)) {
-          if (k == fin.prefix) ++taken;
-          if (pos < kk) {
-            sel[pos] = sc.cand_page[i];
-            sc.out_blk[pos] = sc.cand_blk[i];
+      __syncthreads();
+      const int bin = s_bin;
+      int add_mine = 0, add_before = 0;
+#pragma unroll
+      for (int r = 0; r < kSelCluster; ++r)
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+          if (lo_bin + i > bin) {
+            if (r == rank) add_mine += v[r][i];
+            if (r < rank) add_before += v[r][i];
           }
-          ++pos;
+          if (lo_bin + i == bin) bnd_cnt[r] = v[r][i];
         }
+      block_sum2(add_mine, add_before, scan_buf);   // (ends with a barrier: bnd_cnt is visible)
+      mine += add_mine;
+      before += add_before;
+      bnd[lvl] = (uint32_t)bin;
+      need -= s_above;
+      int inb = 0, low = 0;
+#pragma unroll
+      for (int r = 0; r < kSelCluster; ++r) {
+        inb += bnd_cnt[r];
+        if (r < rank) low += bnd_cnt[r];
+      }
+      if (inb == need || lvl == 2) {
+        // inb == need: the boundary bin is needed whole.  Otherwise (last
+        // level) its keys are equal in all 31 bits: lowest pages first, and
+        // CTAs hold ascending page ranges.
+        final_lvl = lvl;
+        const int take = max(0, min(bnd_cnt[rank], need - low));
+        before += min(low, need);
+        mine += take;
+        if (take == bnd_cnt[rank]) {
+          if (tid == 0) s_cutoff = len;
+        } else if (warp == 0) {
+          // index of this CTA's first boundary key that is not taken
+          int seen = 0, cut = len;
+          for (int base = 0; base < len && cut == len; base += 32) {
+            const int i = base + lane;
+            bool hit = false;
+            if (i < len) {
+              const uint32_t key = sc.keys_s[i];
+              hit = lvl_digit(key, 0) == bnd[0] && lvl_digit(key, 1) == bnd[1] &&
+                    (lvl < 2 || lvl_digit(key, 2) == bnd[2]);
+            }
+            const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+            const int cnt = __popc(bal);
+            if (seen + cnt > take) {
+              uint32_t x = bal;
+              for (int k = 0; k < take - seen; ++k) x &= x - 1u;   // drop the members taken
+              cut = base + __ffs(x) - 1;
+            }
+            seen += cnt;
+          }
+          if (lane == 0) s_cutoff = cut;
+        }
+        __syncthreads();
+        break;
       }
     }
-    if (tid == 0) p.n_selected[unit] = kk;
   }
-  cluster.sync();   // rank 0's out_blk is complete
+  const int cutoff = s_cutoff;
+  const int off = before;   // this CTA's first output slot
+
+  // ---- 4. this CTA's selected pages, ascending, at slots [off, off + mine)
+  {
+    auto taken = [&](uint32_t key, int i) -> bool {
+      if (final_lvl < 0) return (key >> 31) != 0u || lvl_digit(key, 0) > bnd[0];
+      for (int l = 0; l <= final_lvl; ++l) {
+        const uint32_t d = lvl_digit(key, l);
+        if (d != bnd[l]) return d > bnd[l];
+      }
+      return i < cutoff;
+    };
+    const int nchunks = (len + 31) / 32;
+    for (int ch = warp; ch < nchunks; ch += kSelWarps) {   // count per 32-key chunk
+      const int i = ch * 32 + lane;
+      const bool t = i < len && taken(sc.keys_s[i], i);
+      const int cnt = __popc(__ballot_sync(0xffffffffu, t));
+      if (lane == 0) chunk_base[ch] = cnt;
+    }
+    __syncthreads();
+    {
+      // exclusive scan of the chunk counts, two per thread
+      const int a = 2 * tid < nchunks ? chunk_base[2 * tid] : 0;
+      const int c2 = 2 * tid + 1 < nchunks ? chunk_base[2 * tid + 1] : 0;
+      int total;
+      const int ex = block_exclusive_scan(a + c2, scan_buf, total);
+      if (2 * tid < nchunks) chunk_base[2 * tid] = ex;
+      if (2 * tid + 1 < nchunks) chunk_base[2 * tid + 1] = ex + a;
+    }
+    __syncthreads();
+    int* out0 = cluster.map_shared_rank(sc.out_blk, 0);
+    for (int ch = warp; ch < nchunks; ch += kSelWarps) {
+      const int i = ch * 32 + lane;
+      const bool t = i < len && taken(sc.keys_s[i], i);
+      const uint32_t bal = __ballot_sync(0xffffffffu, t);
+      if (t) {
+        const int pos = off + chunk_base[ch] + __popc(bal & ((1u << lane) - 1u));
+        if (pos < kk) {
+          sel[pos] = j0 + i;
+          out0[pos] = sc.bt_slice ? sc.bt_slice[i] : j0 + i;
+        }
+      }
+    }
+  }
+  if (tid == 0 && rank == 0) p.n_selected[unit] = kk;
+  cluster.sync();   // rank 0's out_blk is complete; no CTA reads another's histograms after this
   return res;
 }
 

@@ -24,34 +24,15 @@ constexpr int kGroup = 4;
 constexpr int kRecord = 784;
 constexpr int kTargetCtas = 304;   // 2 resident CTAs x 152 SMs (GB300)
 constexpr int kSelCluster = 8;     // CTAs per (request, KV head) in the selection
-constexpr int kFusedMaxKeysPerCta = 16384; // fused pass: keys + block ids share the 128 KB ring
+constexpr int kFusedMaxKeysPerCta = 16384; // keys per selecting CTA (fused: keys + block ids share the 128 KB ring)
 constexpr int kFusedMaxBudget = 2047;      // fused pass: <= 32 items per warp of 64
-constexpr int kSmemLimit = 216 * 1024;     // dynamic shared memory we allow a CTA (static <= 11 KB)
+constexpr int kSmemLimit = 200 * 1024;     // dynamic shared memory we allow a CTA (static <= 27 KB)
 
-// Entries per CTA in rank 0's candidate arrays (key, page, block: 12 bytes
-// each, kSelCluster segments).  At least min(budget, slice) so that an exact
-// local top-k always fits; up to 2 budget + 64 so that a slice's whole
-// boundary histogram bin usually fits, as far as kSmemLimit leaves room
-// after `fixed` bytes of other dynamic shared memory.
-__host__ __device__ inline int sel_cand_stride(int max_pages, int budget, size_t fixed) {
-  const int slice_cap = (max_pages + kSelCluster - 1) / kSelCluster;
-  const int lo = budget < slice_cap ? budget : slice_cap;
-  long long hi = 2LL * budget + 64;
-  if (hi > slice_cap) hi = slice_cap;
-  const long long fit = fixed < (size_t)kSmemLimit ? (long long)(kSmemLimit - fixed) / (12 * kSelCluster) : 0;
-  if (hi > fit) hi = fit;
-  return hi > lo ? (int)hi : lo;
-}
-
-// Dynamic shared memory of the selection kernel: slice keys, the selected
-// list, then C candidate segments (key, page, block).
-__host__ __device__ inline size_t select_fixed_bytes(int max_pages, int budget) {
+// Dynamic shared memory of the selection kernel: slice keys and the selected
+// list (rank 0).
+__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget) {
   const int slice_cap = (max_pages + kSelCluster - 1) / kSelCluster;
   return 4 * ((size_t)slice_cap + (size_t)budget + 4);
-}
-__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget) {
-  const size_t fixed = select_fixed_bytes(max_pages, budget);
-  return fixed + 12 * (size_t)kSelCluster * sel_cand_stride(max_pages, budget, fixed);
 }
 
 // ---------------------------------------------------------------- status
@@ -200,24 +181,6 @@ __device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// Eight two's-complement int4 codes (one 32-bit word, nibble m at bits 4m)
-// -> four exact f16x2 pairs (nibbles 0|4, 1|5, 2|6, 3|7; low half first).
-// A nibble n at bits 0-3 of a half becomes 0x6400 | (n ^ 8) = 1032 + code;
-// at bits 4-7 it becomes 1024 + 16 (code + 8).  Both are made exact codes by
-// one half2 op.
-__device__ __forceinline__ void nib8_to_h2x4(uint32_t w, uint32_t& p04, uint32_t& p15,
-                                             uint32_t& p26, uint32_t& p37) {
-  const uint32_t w8 = w >> 8;
-  const uint32_t x0 = and_xor(w, 0x000F000Fu, 0x64086408u);
-  const uint32_t x1 = and_xor(w, 0x00F000F0u, 0x64806480u);
-  const uint32_t x2 = and_xor(w8, 0x000F000Fu, 0x64086408u);
-  const uint32_t x3 = and_xor(w8, 0x00F000F0u, 0x64806480u);
-  p04 = h2_sub(x0, 0x64086408u);                 // - 1032
-  p26 = h2_sub(x2, 0x64086408u);
-  p15 = h2_fma(x1, 0x2C002C00u, 0xD480D480u);    // / 16 - 72
-  p37 = h2_fma(x3, 0x2C002C00u, 0xD480D480u);
-}
-
 // Four int8 codes [b0 b1 b2 b3] -> exact f16x2 (b0,b1) and (b2,b3).
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;                        // offset binary
@@ -229,22 +192,28 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
 
 // Biased variants for tensor-core operands whose offset is removed once, in
 // the accumulator's starting value, instead of per element.
-// Eight int4 codes -> four f16x2 pairs of (72 + code), exact: each nibble is
-// moved to bits 4-7 of a half and or-ed under the exponent of 64 (0x5400),
-// where those bits are worth 1 (nibble n ^ 8 = code + 8).
-__device__ __forceinline__ void nib8_to_h2x4_b72(uint32_t w, uint32_t& p04, uint32_t& p15,
-                                                 uint32_t& p26, uint32_t& p37) {
-  p04 = and_xor(w << 4, 0x00F000F0u, 0x54805480u);
+// Eight int4 codes -> four exact f16x2 pairs with one shift and four LOP3s.
+// Nibbles at bits 0-3 of a half (pairs 0|4 and 2|6) sit under the exponent of
+// 64 (0x5400) where a mantissa unit is 1/16: 64 + (n ^ 8)/16 = 64.5 + code/16.
+// Nibbles at bits 4-7 (pairs 1|5 and 3|7) are worth 1 there: 72 + code.  The
+// operand these pairs multiply is scaled by 16 in the low-slot positions, so
+// both kinds contribute code x operand plus a known offset.
+__device__ __forceinline__ void nib8_to_h2x4_biased(uint32_t w, uint32_t& p04, uint32_t& p15,
+                                                    uint32_t& p26, uint32_t& p37) {
+  const uint32_t w8 = w >> 8;
+  p04 = and_xor(w, 0x000F000Fu, 0x54085408u);
   p15 = and_xor(w, 0x00F000F0u, 0x54805480u);
-  p26 = and_xor(w >> 4, 0x00F000F0u, 0x54805480u);
-  p37 = and_xor(w >> 8, 0x00F000F0u, 0x54805480u);
+  p26 = and_xor(w8, 0x000F000Fu, 0x54085408u);
+  p37 = and_xor(w8, 0x00F000F0u, 0x54805480u);
 }
 
-// Four int8 codes [b0 b1 b2 b3] -> f16x2 (1152 + b0, 1152 + b1), (1152 + b2, 1152 + b3).
-__device__ __forceinline__ void i8x4_to_h2x2_b1152(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// Four int8 codes [b0 b1 b2 b3] -> f16x2 (72 + b0/16, 72 + b1/16) for the
+// low-slot (x16-scaled operand) positions and (1152 + b2, 1152 + b3): both
+// multiply their operand into 1152 x q + code x q.
+__device__ __forceinline__ void i8x4_to_h2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  lo = __byte_perm(x, 0x64646464u, 0x4140);
-  hi = __byte_perm(x, 0x64646464u, 0x4342);
+  lo = __byte_perm(x, 0x54545454u, 0x4140);   // 64 + (b + 128)/16
+  hi = __byte_perm(x, 0x64646464u, 0x4342);   // 1024 + b + 128
 }
 
 // fp32 pair -> f16x2 high part and f16x2 residual (x ~= hi + lo to ~2^-22).

@@ -15,7 +15,6 @@ struct ScoreParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   float* scores;      // [batch][H_kv][max_pages][G]
-  float* partials;    // [batch*head_groups][seg_slots][8 warps][G][2]: LSE partial per covering CTA
   uint32_t* status;
   int64_t num_blocks;
   int batch, max_pages, H_kv;
@@ -26,19 +25,15 @@ struct ScoreParams {
   int n_chunks;       // chunks per (b, head group)
   int head_groups;    // H_kv / h_cta
   int n_items;        // batch * head_groups * n_chunks
-  int seg_slots;      // most scoring CTAs one (request, head group) unit's items can span
 };
 
 struct SelectParams {
   const int32_t* seq_lens;
   const float* scores;
-  const float* partials;
   int32_t* selected;       // [batch][H_kv][budget]
   int32_t* n_selected;     // [batch][H_kv]
   uint32_t* status;
   int batch, max_pages, H_kv, budget;
-  // geometry of the scoring pass, to find its partials
-  int score_grid, seg_slots, n_items, n_chunks, head_groups, h_cta, wph;
 };
 
 struct AttnParams {

@@ -35,17 +35,11 @@ constexpr int kFusedRing = kFusedWarps * kFusedStages * kStageBytes;   // 128 KB
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Dynamic shared memory: [ring (keys and block ids of the slice during the
-// selection)] [candidates: keys, pages, blocks] [selected blocks] [barriers]
-__host__ __device__ inline int fused_cand_stride(int max_pages, int budget) {
-  const size_t fixed = 1024 + kFusedRing + 4 * (size_t)budget + 16 + kFusedWarps * kFusedStages * 8;
-  return sel_cand_stride(max_pages, budget, fixed);
-}
-__host__ __device__ inline size_t fused_cand_bytes(int max_pages, int budget) {
-  const int stride = fused_cand_stride(max_pages, budget);
-  return ((12 * (size_t)kSelCluster * stride + 4 * (size_t)budget) + 15) / 16 * 16;
-}
+// selection)] [selected blocks (rank 0)] [barriers]
+__host__ __device__ inline size_t fused_list_bytes(int budget) { return (4 * (size_t)budget + 15) / 16 * 16; }
 size_t fused_smem_bytes(int max_pages, int budget) {
-  return 1024 + kFusedRing + fused_cand_bytes(max_pages, budget) + kFusedWarps * kFusedStages * 8;
+  (void)max_pages;   // the slice's keys and block ids live in the ring (host limits their size)
+  return 1024 + kFusedRing + fused_list_bytes(budget) + kFusedWarps * kFusedStages * 8;
 }
 
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 1)
@@ -54,9 +48,8 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   extern __shared__ uint8_t fused_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fused_raw) + 1023) & ~uintptr_t(1023));
   const int slice_cap = (p.sel.max_pages + kSelCluster - 1) / kSelCluster;
-  const int stride = fused_cand_stride(p.sel.max_pages, p.sel.budget);
-  uint32_t* cand = reinterpret_cast<uint32_t*>(smem + kFusedRing);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFusedRing + fused_cand_bytes(p.sel.max_pages, p.sel.budget));
+  int* list = reinterpret_cast<int*>(smem + kFusedRing);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFusedRing + fused_list_bytes(p.sel.budget));
   __shared__ int stage_valid[kFusedWarps][kFusedStages];
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -93,17 +86,13 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
   __syncthreads();
 
-  griddep_wait();   // scores and partials of the scoring pass are now visible
+  griddep_wait();   // the scoring pass's scores are now visible
 
   // ---- selection (the ring holds this CTA's keys and block ids meanwhile)
   SelScratch sc;
   sc.keys_s = reinterpret_cast<uint32_t*>(smem);
   sc.bt_slice = bt_slice;
-  sc.cand_key = cand;
-  sc.cand_page = reinterpret_cast<int*>(cand + kSelCluster * stride);
-  sc.cand_blk = sc.cand_page + kSelCluster * stride;
-  sc.cand_stride = stride;
-  sc.out_blk = sc.cand_blk + kSelCluster * stride;
+  sc.out_blk = list;
   const ClusterSel cs = cluster_select(p.sel, sc);
   fence_proxy_async_smem();   // generic writes to the ring before the tensor copies reuse it
   __syncthreads();
