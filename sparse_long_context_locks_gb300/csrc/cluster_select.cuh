@@ -152,7 +152,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   __shared__ float zl[kGroup];
   __shared__ int scan_buf[32];
   __shared__ int bnd_cnt[kSelCluster];         // per-CTA count in the boundary bin
-  __shared__ int s_bin, s_above, s_bt_mine, s_bt_before, s_cutoff, s_cnt;
+  __shared__ int s_bin, s_above, s_cutoff, s_cnt;
   __shared__ int chunk_base[kSelMaxChunks];
 
   cg::cluster_group cluster = cg::this_cluster();

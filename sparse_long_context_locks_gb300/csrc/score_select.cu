@@ -244,11 +244,21 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
         if (it < it_end) enter_unit();
       }
     };
-    if (it < it_end) enter_unit();
-    skip_empty();
     int64_t blk = -1;
-    if (it < it_end && lane < kPps && c * kPps + lane < n)
-      blk = p.block_table[(int64_t)b * p.max_pages + c * kPps + lane];
+    if (it < it_end) {
+      // the first stage's block ids are fetched alongside the sequence length
+      const int pg0 = c * kPps + lane;
+      if (lane < kPps && pg0 < p.max_pages)
+        blk = p.block_table[(int64_t)(first_unit / p.head_groups) * p.max_pages + pg0];
+      enter_unit();
+    }
+    const int it0 = it;
+    skip_empty();
+    if (it != it0 || !(lane < kPps && c * kPps + lane < n)) {
+      blk = -1;
+      if (it < it_end && lane < kPps && c * kPps + lane < n)
+        blk = p.block_table[(int64_t)b * p.max_pages + c * kPps + lane];
+    }
     while (it < it_end && ok) {
       const int s = step % kScoreStages;
       if (step >= kScoreStages) ok = mbar_wait(&empty[s], ((step / kScoreStages) - 1) & 1, p.status);
