@@ -31,6 +31,11 @@ namespace locks {
 constexpr int kFusedWarps = kSelThreads / 32;                  // 8
 constexpr int kFusedStages = 2;
 constexpr int kFusedRing = kFusedWarps * kFusedStages * kStageBytes;   // 128 KB
+// Warps 0 and 1 own a third stage (after the ring), so a unit of up to 130
+// items (128 selected pages and the tail) is read in one round of copies.
+constexpr int kFusedExtraWarps = 2;
+constexpr int kFusedMaxStages = kFusedStages + 1;
+constexpr int kFusedExtra = kFusedExtraWarps * kStageBytes;             // 16 KB
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -39,7 +44,7 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __host__ __device__ inline size_t fused_list_bytes(int budget) { return (4 * (size_t)budget + 15) / 16 * 16; }
 size_t fused_smem_bytes(int max_pages, int budget) {
   (void)max_pages;   // the slice's keys and block ids live in the ring (host limits their size)
-  return 1024 + kFusedRing + fused_list_bytes(budget) + kFusedWarps * kFusedStages * 8;
+  return 1024 + kFusedRing + kFusedExtra + fused_list_bytes(budget) + kFusedWarps * kFusedMaxStages * 8;
 }
 
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 1)
@@ -48,22 +53,25 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   extern __shared__ uint8_t fused_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fused_raw) + 1023) & ~uintptr_t(1023));
   const int slice_cap = (p.sel.max_pages + kSelCluster - 1) / kSelCluster;
-  int* list = reinterpret_cast<int*>(smem + kFusedRing);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFusedRing + fused_list_bytes(p.sel.budget));
-  __shared__ int stage_valid[kFusedWarps][kFusedStages];
+  int* list = reinterpret_cast<int*>(smem + kFusedRing + kFusedExtra);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFusedRing + kFusedExtra + fused_list_bytes(p.sel.budget));
+  __shared__ int stage_valid[kFusedWarps][kFusedMaxStages];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.y;
   const int b = unit / p.sel.H_kv, h = unit % p.sel.H_kv;
-  uint64_t* mybar = bars + warp * kFusedStages;
-  uint8_t* ring_ptr = smem + warp * kFusedStages * kStageBytes;
-  const uint32_t ring = smem_u32(ring_ptr);
+  uint64_t* mybar = bars + warp * kFusedMaxStages;
+  const int nst = warp < kFusedExtraWarps ? kFusedMaxStages : kFusedStages;   // this warp's stages
+  auto stage_ptr = [&](int st) -> uint8_t* {
+    return st < kFusedStages ? smem + (warp * kFusedStages + st) * kStageBytes
+                             : smem + kFusedRing + warp * kStageBytes;
+  };
 
   // ---- prologue: independent of the scoring pass's results
   if (lane == 0) {
-    for (int s = 0; s < kFusedStages; ++s) mbar_init(&mybar[s], 1);
+    for (int s = 0; s < nst; ++s) mbar_init(&mybar[s], 1);
     fence_mbar_init();
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
@@ -120,9 +128,9 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
       valid = 0;
     }
   }
-  if (lane < min(kFusedStages, my_count)) {
+  if (lane < min(nst, my_count)) {
     stage_valid[warp][lane] = valid;
-    attn_issue_page(&tmk, &tmv, ring_ptr + lane * kStageBytes, &mybar[lane], blk, p.sel.H_kv, h);
+    attn_issue_page(&tmk, &tmv, stage_ptr(lane), &mybar[lane], blk, p.sel.H_kv, h);
   }
   __syncwarp();
 
@@ -130,21 +138,20 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   attn_init(st);
   bool ok = true;
   for (int k = 0; k < my_count; ++k) {
-    const int stage = k % kFusedStages;
-    if (ok) ok = mbar_wait(&mybar[stage], (k / kFusedStages) & 1, p.sel.status);
+    const int stage = k % nst;
+    if (ok) ok = mbar_wait(&mybar[stage], (k / nst) & 1, p.sel.status);
     const int v = stage_valid[warp][stage];
-    if (ok && v > 0)
-      attn_page(st, ring + stage * kStageBytes, ring_ptr + stage * kStageBytes + kTileBytes, v, qb, p.scale_log2,
-                lane);
+    uint8_t* sp = stage_ptr(stage);
+    if (ok && v > 0) attn_page(st, smem_u32(sp), sp + kTileBytes, v, qb, p.scale_log2, lane);
     fence_proxy_async_smem();
     __syncwarp();
-    const int kn = k + kFusedStages;
+    const int kn = k + nst;
     if (kn < my_count) {
       const int64_t nb = __shfl_sync(0xffffffffu, blk, kn);
       const int nv = __shfl_sync(0xffffffffu, valid, kn);
       if (lane == 0) {
         stage_valid[warp][stage] = nv;
-        attn_issue_page(&tmk, &tmv, ring_ptr + stage * kStageBytes, &mybar[stage], nb, p.sel.H_kv, h);
+        attn_issue_page(&tmk, &tmv, sp, &mybar[stage], nb, p.sel.H_kv, h);
       }
     }
     __syncwarp();
