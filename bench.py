@@ -1,11 +1,13 @@
 """Decode-step benchmark of the LOCKS hot path on GB300.
 
 A step is one pass of the decode hot path over one batch of synthetic input:
-locks_decode_step = page scoring (locks_score) followed by the fused cluster
-kernel of locks_select_sparse_decode (group-shared top-k selection and sparse
-paged attention over the selected pages and the open tail page), captured once
-into a CUDA graph and replayed.  The separate selection and split-K sparse
-attention kernels are timed too (rows "select_us", "sparse_attention_us").  The
+locks_decode_step = page scoring (locks_score) followed by group-shared top-k
+selection and sparse paged attention over the selected pages and the open tail
+page -- one fused cluster kernel when every (request, KV head) cluster fits on
+the GPU at once, else the selection kernel and split-K attention -- captured
+once into a CUDA graph and replayed.  The fused and the separate kernels are
+also timed on their own (rows "select_attend_fused_us", "select_us",
+"sparse_attention_us").  The
 summary builder (run when pages are finalised, off the decode critical path)
 and the dense comparator are timed in the same run and reported under "rows".
 
@@ -384,6 +386,13 @@ def main():
                               "clocks": ClockSampler.summary(clock_rows)}))
         return
 
+    # locks_decode_step runs the fused cluster kernel when every (request, KV
+    # head) cluster of 8 CTAs fits on the GPU at once, else selection + split-K
+    n_sms = torch.cuda.get_device_properties(local).multi_processor_count
+    fused_path = B * H * 8 <= n_sms
+    launches_per_step = 2 if fused_path else 3
+    config["step_path"] = "score + fused select/attend" if fused_path else "score + select + split-K attend"
+
     # ---------------------------------------------------------------- per-kernel rows
     R = min(200, max(20, K // 10))
 
@@ -475,7 +484,7 @@ def main():
                 "d2h_bytes_per_step": d2h,
                 "mode": "pinned H2D of q and seq_lens, graph replay of locks_decode_step, "
                         "D2H of out, host wall clock incl. stream sync"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step * K,
         "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs, "peak": peak,
                      "unit": "GB/s", "frac": score_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": by["score"], "peak_source": peak_src},

@@ -206,9 +206,12 @@ locks_status locks_select_sparse_decode(const locks_cfg *cfg, const void *q, con
                                         float sm_scale, float *out, void *workspace,
                                         size_t workspace_bytes, locks_stream_t stream);
 
-/* One whole LOCKS decode step for a batch: locks_score then
- * locks_select_sparse_decode on `stream` (two kernels, the second a
- * programmatic dependent of the first).  Same limits as the fused call. */
+/* One whole LOCKS decode step for a batch: locks_score, then either
+ * locks_select_sparse_decode (when batch * num_kv_heads clusters of 8 CTAs
+ * fit on the GPU at once; the second kernel is a programmatic dependent of
+ * the first) or locks_select followed by locks_sparse_decode (larger
+ * batches, where the cluster kernel would run in many waves).  Same results
+ * either way; same limits as the fused call. */
 locks_status locks_decode_step(const locks_cfg *cfg, const void *q, const void *summaries,
                                const void *k_cache, const void *v_cache, int64_t num_blocks,
                                const int32_t *block_table, const int32_t *seq_lens, int32_t batch,

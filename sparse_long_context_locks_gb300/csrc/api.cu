@@ -88,6 +88,19 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device (queried once per device; host only).
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 #define LOCKS_CHECK_PTR(p) \
   do {                     \
     if ((p) == nullptr || !aligned16(p)) return LOCKS_ERR_INVALID_ARG; \
@@ -383,9 +396,19 @@ locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* 
   locks_status st = locks_score(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores,
                                 workspace, workspace_bytes, stream);
   if (st != LOCKS_OK) return st;
-  return locks_select_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, batch, max_pages,
-                                    budget_pages, scores, selected, n_selected, sm_scale, out, workspace,
-                                    workspace_bytes, stream);
+  // One cluster per (request, KV head): when they all fit on the GPU at once
+  // the fused kernel keeps the selection on chip; with more units its
+  // latency-bound clusters would run in many waves, so the selection kernel
+  // (small CTAs, many resident per SM) and the split-K attention run instead.
+  if ((int64_t)batch * cfg->num_kv_heads * kSelCluster <= num_sms())
+    return locks_select_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, batch, max_pages,
+                                      budget_pages, scores, selected, n_selected, sm_scale, out, workspace,
+                                      workspace_bytes, stream);
+  st = locks_select(cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected, workspace,
+                    workspace_bytes, stream);
+  if (st != LOCKS_OK) return st;
+  return locks_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, selected, n_selected,
+                             batch, max_pages, budget_pages, sm_scale, out, workspace, workspace_bytes, stream);
 }
 
 locks_status locks_score_select(const locks_cfg* cfg, const void* q, const void* summaries,
