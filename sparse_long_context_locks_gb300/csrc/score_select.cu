@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // ---------------------------------------------------------------- select
 
 
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 1)
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 4)
     select_kernel(const SelectParams p) {
   // [slice keys][selected list]
   extern __shared__ __align__(16) uint32_t sel_dyn[];
