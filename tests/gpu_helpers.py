@@ -33,7 +33,8 @@ CODE_EDGE = 0.02
 class Run:
     """One decode step of a workload on the GPU, with every intermediate kept."""
 
-    def __init__(self, w: W.Workload, tail_fill="zero", build=True, dense=False, data=None, fused=False):
+    def __init__(self, w: W.Workload, tail_fill="zero", build=True, dense=False, data=None, fused=False,
+                 step=False):
         self.w = w
         self.d = data if data is not None else W.generate(w, device="cuda", tail_fill=tail_fill)
         d = self.d
@@ -57,13 +58,24 @@ class Run:
                                  d["seq_lens"], self.dense_out, self.bufs.workspace)
         self.fused = None
         if fused:
+            # the fused cluster kernel itself, on the scores locks_score wrote
+            f = {"selected": torch.full_like(self.bufs.selected, -1),
+                 "n_selected": torch.full_like(self.bufs.n_selected, -1),
+                 "out": torch.full_like(self.bufs.out, float("nan"))}
+            L.locks_select_sparse_decode(H, d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                         d["seq_lens"], w.budget_pages, f["selected"], f["n_selected"],
+                                         f["out"], self.bufs.workspace, scores=self.bufs.scores)
+            self.fused = f
+        self.step = None
+        if step:
+            # the whole step through locks_decode_step (either path)
             f = {"selected": torch.full_like(self.bufs.selected, -1),
                  "n_selected": torch.full_like(self.bufs.n_selected, -1),
                  "out": torch.full_like(self.bufs.out, float("nan"))}
             L.locks_decode_step(H, d["q"], self.summ, d["k_cache"], d["v_cache"], d["block_table"],
                                 d["seq_lens"], w.budget_pages, f["selected"], f["n_selected"],
                                 f["out"], self.bufs.workspace)
-            self.fused = f
+            self.step = f
         torch.cuda.synchronize()
         self.status = L.locks_read_status(self.bufs.workspace)
         self.lens = d["seq_lens"].cpu().tolist()
@@ -223,11 +235,12 @@ def check_records(gpu_rec: np.ndarray, K_pages: np.ndarray) -> dict:
     return {"pages": P, "well_conditioned": n_well}
 
 
-def check_fused_unit(run: Run, b: int, h: int):
-    """The fused select + attend pass selects exactly what locks_select does
-    (same scores, same selection) and its output matches the oracle's
-    attention over that selection."""
-    f = run.fused
+def check_fused_unit(run: Run, b: int, h: int, which: str = "fused"):
+    """The fused select + attend pass (which="fused") or the whole decode step
+    (which="step") selects exactly what locks_select does (same scores, same
+    selection) and its output matches the oracle's attention over that
+    selection."""
+    f = run.fused if which == "fused" else run.step
     ns = int(f["n_selected"][b, h])
     sel_f = f["selected"][b, h, :ns].cpu().numpy().astype(np.int64)
     assert sel_f.tolist() == run.gpu_selected(b, h).tolist()

@@ -1,6 +1,8 @@
-"""The fused decode step (locks_decode_step = locks_score followed by the
-cluster kernel of locks_select_sparse_decode) against the separate calls and
-the fp64 oracle, on small edge cases and on the named workloads."""
+"""The fused select + attend cluster kernel (locks_select_sparse_decode) and
+the whole decode step (locks_decode_step, which uses that kernel when every
+unit's cluster fits on the GPU at once and the selection kernel plus split-K
+attention otherwise) against the separate calls and the fp64 oracle, on small
+edge cases and on the named workloads."""
 
 import numpy as np
 import pytest
@@ -38,18 +40,31 @@ def test_fused_matches_separate_and_oracle(ctx, heads, budget):
 
 def test_fused_ragged_batch_and_ties():
     w = _w(batch=4, context=16 * 90, context_hi=16 * 700, budget_tokens=16 * 40, seed=5)
-    run = Run(w, tail_fill="huge", fused=True)
+    run = Run(w, tail_fill="huge", fused=True, step=True)
     assert run.status == 0
     for b in range(4):
         for h in (0, 7):
             check_fused_unit(run, b, h)
+            check_fused_unit(run, b, h, which="step")   # 32 units x 8 CTAs: the separate path
+
+
+@pytest.mark.parametrize("batch,heads", [(1, 8), (2, 8), (19, 1), (20, 8)])
+def test_decode_step_both_paths(batch, heads):
+    # batch x heads x 8 CTAs <= 152 SMs takes the fused kernel, more the separate path
+    w = _w(batch=batch, num_kv_heads=heads, context=16 * 120, context_hi=16 * 400,
+           budget_tokens=16 * 32, seed=batch + heads)
+    run = Run(w, tail_fill="nan", step=True)
+    assert run.status == 0
+    for b in sorted({0, batch // 2, batch - 1}):
+        for h in sorted({0, heads - 1}):
+            check_fused_unit(run, b, h, which="step")
 
 
 def test_fused_step_in_a_graph_is_stable():
     w = _w(context=16 * 800 + 5, seed=9)
-    run = Run(w, fused=True)
-    first = run.fused["out"].clone()
-    d, H, bufs, f = run.d, run.H, run.bufs, run.fused
+    run = Run(w, step=True)
+    first = run.step["out"].clone()
+    d, H, bufs, f = run.d, run.H, run.bufs, run.step
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         L.locks_decode_step(H, d["q"], run.summ, d["k_cache"], d["v_cache"], d["block_table"],
