@@ -421,6 +421,19 @@ def main():
     g_build = capture(build_all)
     us_build = time_graph(g_build, reps=max(5, R // 10))
     n_page_heads = int(blocks.numel()) * H
+    # page crossing: one page per request became full (stand-in: B distinct
+    # full blocks), built from a device-side count, alone and ahead of a step
+    pend_ids = blocks[:B].to(torch.int32).contiguous()
+    n_pend = torch.full((1,), int(pend_ids.numel()), dtype=torch.int32, device="cuda")
+    g_pend = capture(lambda s: L.locks_build_pending(H, data["k_cache"], pend_ids, n_pend, summ,
+                                                     bufs.workspace, stream=s))
+    us_pend = time_graph(g_pend)
+
+    def crossing_step(s):
+        L.locks_build_pending(H, data["k_cache"], pend_ids, n_pend, summ, bufs.workspace, stream=s)
+        step_calls(s)
+    g_cross = capture(crossing_step)
+    us_cross = time_graph(g_cross)
 
     peak, peak_src = peaks()
     score_gbs = by["score"] / (us_score * 1e-6) / 1e9
@@ -497,6 +510,8 @@ def main():
             "dense_us": us_dense, "dense_GBps": by["dense_kv"] / (us_dense * 1e-6) / 1e9,
             "dense_frac": by["dense_kv"] / (us_dense * 1e-6) / 1e9 / peak,
             "build_us": us_build, "build_page_heads": n_page_heads,
+            "build_pending_us": us_pend, "build_pending_page_heads": int(pend_ids.numel()) * H,
+            "step_with_page_crossing_us": us_cross,
             "build_GBps": (n_page_heads * (4096 + 784)) / (us_build * 1e-6) / 1e9,
             "bytes_step": by["step"], "bytes_dense": by["dense_step"],
             "bytes_ratio_dense_over_step": by["dense_step"] / by["step"],

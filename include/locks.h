@@ -142,6 +142,20 @@ locks_status locks_build_summaries(const locks_cfg *cfg, const void *k_cache, in
                                    const int32_t *block_ids, int32_t n_build, void *summaries,
                                    void *workspace, size_t workspace_bytes, locks_stream_t stream);
 
+/* Page-crossing build, §2 "page-local spectral decomposition" ("when a page
+ * is finalised") and "implementation" (full CUDA graph): the same records as
+ * locks_build_summaries for block_ids[0, min(*n_pending, max_pending)), where
+ * n_pending points to a device int32 that the kernel reads.  One captured
+ * graph thus serves every decode step, whatever number of requests crossed a
+ * page boundary at that step (at most max_pending, e.g. one per request).
+ * Entries at or past *n_pending are not read.  Launch it before
+ * locks_decode_step on the same stream so the newly full pages are scored.
+ * n_pending must be 4-byte aligned. */
+locks_status locks_build_pending(const locks_cfg *cfg, const void *k_cache, int64_t num_blocks,
+                                 const int32_t *block_ids, const int32_t *n_pending, int32_t max_pending,
+                                 void *summaries, void *workspace, size_t workspace_bytes,
+                                 locks_stream_t stream);
+
 /* Scoring pass, §2 "reconstruction and selection" (the s_j(q) equation):
  * for every request b, KV head h and full page j < n_b, read the page's
  * record (and nothing else of the cache) and write, for each query head g of

@@ -253,6 +253,31 @@ locks_status locks_build_summaries(const locks_cfg* cfg, const void* k_cache, in
   return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+locks_status locks_build_pending(const locks_cfg* cfg, const void* k_cache, int64_t num_blocks,
+                                 const int32_t* block_ids, const int32_t* n_pending, int32_t max_pending,
+                                 void* summaries, void* workspace, size_t workspace_bytes,
+                                 locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (max_pending < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
+  if (max_pending == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(k_cache);
+  LOCKS_CHECK_PTR(block_ids);
+  LOCKS_CHECK_PTR(summaries);
+  if (n_pending == nullptr || (reinterpret_cast<uintptr_t>(n_pending) & 3u) != 0) return LOCKS_ERR_INVALID_ARG;
+  if (workspace != nullptr && (!aligned16(workspace) || workspace_bytes < sizeof(uint32_t)))
+    return LOCKS_ERR_INVALID_ARG;
+  BuildParams p{};
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.block_ids = block_ids;
+  p.n_dev = n_pending;
+  p.summ = static_cast<uint8_t*>(summaries);
+  p.status = status_word(workspace);
+  p.num_blocks = num_blocks;
+  p.n_build = max_pending;
+  p.H_kv = cfg->num_kv_heads;
+  return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summaries, int64_t num_blocks,
                          const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
                          int32_t max_pages, float* scores, void* workspace, size_t workspace_bytes,

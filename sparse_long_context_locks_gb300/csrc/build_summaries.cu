@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_b)[warp * 2 + half];
 
   const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;   // page-head index
-  const int64_t total = (int64_t)p.n_build * p.H_kv;
+  const int n_pages = p.n_dev != nullptr ? min(p.n_build, max(0, *p.n_dev)) : p.n_build;
+  const int64_t total = (int64_t)n_pages * p.H_kv;
   bool active = ph < total;
   int64_t blk = -1;
   int h = 0;

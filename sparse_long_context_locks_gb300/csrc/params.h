@@ -56,6 +56,7 @@ struct AttnParams {
 struct BuildParams {
   const __nv_bfloat16* k_cache;
   const int32_t* block_ids;
+  const int32_t* n_dev;    // optional device count: build block_ids[0, min(n_build, *n_dev))
   uint8_t* summ;
   uint32_t* status;
   int64_t num_blocks;

@@ -50,6 +50,7 @@ _SIGS = {
     "locks_workspace_init": (_I32, [_P, _SZ, _P]),
     "locks_read_status": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "locks_build_summaries": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _SZ, _P]),
+    "locks_build_pending": (_I32, [_CFG, _P, _I64, _P, _P, _I32, _P, _P, _SZ, _P]),
     "locks_score": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _SZ, _P]),
     "locks_select": (_I32, [_CFG, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "locks_score_select": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _P, _P, _P,
@@ -146,6 +147,18 @@ def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace
         ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), block_ids.numel(),
         _ptr(summaries), _ptr(workspace), _nbytes(workspace), _stream(stream)),
         "locks_build_summaries")
+
+
+def locks_build_pending(num_kv_heads, k_cache, block_ids, n_pending, summaries, workspace=None,
+                        stream=None):
+    """Build the records of block_ids[0, n_pending[0]) (n_pending: a device
+    int32 tensor, read by the kernel); block_ids holds room for the most pages
+    any step can finalise."""
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_build_pending(
+        ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), _ptr(n_pending),
+        block_ids.numel(), _ptr(summaries), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_build_pending")
 
 
 def locks_score(num_kv_heads, q, summaries, block_table, seq_lens, workspace, scores=None,

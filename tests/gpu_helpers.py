@@ -34,15 +34,16 @@ class Run:
     """One decode step of a workload on the GPU, with every intermediate kept."""
 
     def __init__(self, w: W.Workload, tail_fill="zero", build=True, dense=False, data=None, fused=False,
-                 step=False):
+                 step=False, summ=None):
         self.w = w
         self.d = data if data is not None else W.generate(w, device="cuda", tail_fill=tail_fill)
         d = self.d
         H = w.num_kv_heads
         self.H = H
-        self.summ = torch.zeros(d["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
+        self.summ = summ if summ is not None else torch.zeros(d["num_blocks"], H, 784, dtype=torch.uint8,
+                                                              device="cuda")
         self.bufs = L.DecodeBuffers(H, w.batch, w.max_pages, w.budget_pages)
-        if build:
+        if build and summ is None:
             blocks = W.full_page_blocks(d).cuda()
             L.locks_build_summaries(H, d["k_cache"], blocks, self.summ, self.bufs.workspace)
         L.locks_score_select(H, d["q"], self.summ, d["block_table"], d["seq_lens"], w.budget_pages,
