@@ -62,9 +62,14 @@ __device__ __forceinline__ void jacobi_round(float (&g)[kPage], float (&w)[kPage
   const float bb = S.G[hi * kPage + hi];
   const float e = S.G[lo * kPage + hi];
   float c = 1.f, s = 0.f;
-  if (fabsf(e) > 1e-30f && fabsf(e) > 1e-12f * sqrtf(fabsf(a * bb))) {
-    const float tau = (bb - a) / (2.f * e);
-    const float t = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+  // (approximate division and square root: c and s are renormalised from t,
+  // so the rotation stays orthogonal whatever t's rounding)
+  if (fabsf(e) > 1e-30f && e * e > 1e-24f * fabsf(a * bb)) {
+    // |tau| beyond 1e18 gives a rotation below 1e-18: clamped so 1 + tau^2
+    // stays finite
+    const float tau = fminf(fmaxf(__fdividef(bb - a, 2.f * e), -1e18f), 1e18f);
+    const float r2 = 1.f + tau * tau;
+    const float t = __fdividef(copysignf(1.f, tau), fabsf(tau) + r2 * rsqrtf(r2));
     c = rsqrtf(1.f + t * t);
     s = t * c;
   }
@@ -205,9 +210,12 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   for (int j = 0; j < kPage; j += 4)
     *reinterpret_cast<float4*>(&S.W[i * kPage + j]) = make_float4(w[j], w[j + 1], w[j + 2], w[j + 3]);
   __syncwarp();
-  float lam[kPage];
+  float lam[kPage];   // (a NaN would break the ranking below: it ranks last)
 #pragma unroll
-  for (int j = 0; j < kPage; ++j) lam[j] = S.G[j * kPage + j];
+  for (int j = 0; j < kPage; ++j) {
+    const float v = S.G[j * kPage + j];
+    lam[j] = v == v ? v : -INFINITY;
+  }
   const float my_lam = lam[i];
   int rank = 0;
   float lam1 = lam[0];
@@ -287,12 +295,17 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
   }
   const float sV = vmax / 7.f, sM = mmax / 127.f, sC = cmax / 127.f;
+  // codes = round-half-even(x / s) taken as x * (1 / s): one rounding more,
+  // which moves a code only for a quotient within an ulp of a half
+  const float iV = sV > 0.f ? __frcp_rn(sV) : 0.f;
+  const float iM = sM > 0.f ? __frcp_rn(sM) : 0.f;
+  const float iC = sC > 0.f ? __frcp_rn(sC) : 0.f;
   // V codes -> [k][dim] bytes
 #pragma unroll
   for (int e = 0; e < 8; ++e)
 #pragma unroll
     for (int k = 0; k < kRank; ++k) {
-      int c = sV > 0.f ? __float2int_rn(__fdiv_rn(V[e][k], sV)) : 0;
+      int c = __float2int_rn(V[e][k] * iV);
       c = max(-7, min(7, c));
       S.vcode[k * kHeadDim + 8 * i + e] = (int8_t)c;
     }
@@ -300,7 +313,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int dim = 8 * i + e;
-    int c = sM > 0.f ? __float2int_rn(__fdiv_rn(mu8[e], sM)) : 0;
+    int c = __float2int_rn(mu8[e] * iM);
     c = max(-127, min(127, c));
     const int s = dim >> 4, wd = dim & 15, hh = wd >> 3, t = (wd & 7) >> 1, ee = wd & 1;
     S.rec[512 + t * 32 + s * 4 + hh * 2 + ee] = (uint8_t)(int8_t)c;
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // coefficient codes of token i
 #pragma unroll
   for (int k = 0; k < kRank; ++k) {
-    int c = sC > 0.f ? __float2int_rn(__fdiv_rn(crow[k], sC)) : 0;
+    int c = __float2int_rn(crow[k] * iC);
     c = max(-127, min(127, c));
     const int nt = i >> 3, gd = i & 7, tk = k >> 1, ek = k & 1;
     S.rec[640 + (gd * 4 + tk) * 4 + nt * 2 + ek] = (uint8_t)(int8_t)c;

@@ -144,8 +144,14 @@ def test_pipeline_exact_ties_go_to_lower_page_index():
         d["k_cache"][int(bt[0, j])] = d["k_cache"][src]
     run = Run(w, data=d)
     s = run.gpu_scores(0, 0)
+    # identical records (the builder is deterministic) ...
+    r3 = run.summ[int(bt[0, 3]), 0]
     for j in copies:
-        assert np.array_equal(s[j], s[3])
+        assert torch.equal(run.summ[int(bt[0, j]), 0], r3)
+    # ... and scores equal up to the scorer's rounding, which depends on a
+    # page's slot within its group of four (a last-bit difference at most)
+    for j in copies:
+        np.testing.assert_allclose(s[j], s[3], rtol=1e-6, atol=0)
     sel = run.gpu_selected(0, 0).tolist()
     assert sel == [3, 7, 12, 30, 35]
     check_unit(run, 0, 0)
