@@ -219,6 +219,20 @@ def dist_env():
     return world, rank, local
 
 
+def job_step_and_throughput(ms_step: float, world: int, batch: int, device=None):
+    """Whole-job step time and throughput for `world` independent replicas
+    (weak scaling): the slowest rank's mean step time, and every rank's batch
+    over it.  Collective over the default process group when world > 1."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        ms_step = float(t.item())
+    return ms_step, world * batch / (ms_step * 1e-3)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -371,13 +385,7 @@ def main():
     t_wall = time.perf_counter() - t_wall0
     clock_rows = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_step = sum(step_ms) / K
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        ms_step = float(t.item())
-    value = world * B / (ms_step * 1e-3)
+    ms_step, value = job_step_and_throughput(sum(step_ms) / K, world, B, device="cuda")
     if args.profile_run:
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
