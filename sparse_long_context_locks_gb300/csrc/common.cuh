@@ -190,37 +190,27 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
   hi = h2_sub(b, 0x64806480u);
 }
 
-// Biased variants for tensor-core operands whose offset is removed once, in
-// the accumulator's starting value, instead of per element.
-// Eight int4 codes -> four exact f16x2 pairs with one shift and four LOP3s.
-// Nibbles at bits 0-3 of a half (pairs 0|4 and 2|6) sit under the exponent of
-// 64 (0x5400) where a mantissa unit is 1/16: 64 + (n ^ 8)/16 = 64.5 + code/16.
-// Nibbles at bits 4-7 (pairs 1|5 and 3|7) are worth 1 there: 72 + code.  The
-// operand these pairs multiply is scaled by 16 in the low-slot positions, so
-// both kinds contribute code x operand plus a known offset.
-__device__ __forceinline__ void nib8_to_h2x4_biased(uint32_t w, uint32_t& p04, uint32_t& p15,
-                                                    uint32_t& p26, uint32_t& p37) {
+// Eight int4 codes (two's complement nibbles) -> four exact f16x2 pairs, one
+// shift, four LOP3s and four HSUB2s.  A nibble at bits 0-3 of a half (pairs
+// 0|4 and 2|6) goes under the exponent of 1024, where a mantissa unit is 1:
+// 1024 + (n ^ 8) - 1032 = code.  A nibble at bits 4-7 (pairs 1|5 and 3|7)
+// goes under the exponent of 64, where bit 4 is worth 1: 64 + (n ^ 8) - 72.
+// Exact values keep the tensor-core accumulators free of large offsets, whose
+// cancellation would cost precision in proportion to |q|.
+__device__ __forceinline__ void nib8_to_h2x4(uint32_t w, uint32_t& p04, uint32_t& p15, uint32_t& p26,
+                                             uint32_t& p37) {
   const uint32_t w8 = w >> 8;
-  p04 = and_xor(w, 0x000F000Fu, 0x54085408u);
-  p15 = and_xor(w, 0x00F000F0u, 0x54805480u);
-  p26 = and_xor(w8, 0x000F000Fu, 0x54085408u);
-  p37 = and_xor(w8, 0x00F000F0u, 0x54805480u);
-}
-
-// Four int8 codes [b0 b1 b2 b3] -> f16x2 (72 + b0/16, 72 + b1/16) for the
-// low-slot (x16-scaled operand) positions and (1152 + b2, 1152 + b3): both
-// multiply their operand into 1152 x q + code x q.
-__device__ __forceinline__ void i8x4_to_h2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  lo = __byte_perm(x, 0x54545454u, 0x4140);   // 64 + (b + 128)/16
-  hi = __byte_perm(x, 0x64646464u, 0x4342);   // 1024 + b + 128
+  p04 = h2_sub(and_xor(w, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  p15 = h2_sub(and_xor(w, 0x00F000F0u, 0x54805480u), 0x54805480u);
+  p26 = h2_sub(and_xor(w8, 0x000F000Fu, 0x64086408u), 0x64086408u);
+  p37 = h2_sub(and_xor(w8, 0x00F000F0u, 0x54805480u), 0x54805480u);
 }
 
 // fp32 pair -> f16x2 high part and f16x2 residual (x ~= hi + lo to ~2^-22).
 __device__ __forceinline__ void split_h2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(x0, x1);
   const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  const __half2 l = __floats2half2_rn(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }

@@ -14,11 +14,15 @@
 // tensor cores as three small dense contractions:
 //   u  = V^T q     m16n8k16 f16: rows = (2 pages x 8 directions), cols = the
 //                  4 query heads (duplicated to 8), K = 128 dims; A comes
-//                  straight from the int4 codes (one 16-byte load per lane);
-//   q.mu           m16n8k16 f16: rows = the 4 pages' int8 centroids;
+//                  from the int4 codes (one 16-byte load per lane), each
+//                  converted to its exact f16 value;
+//   q.mu           m16n8k16 f16 over K = 64: rows 0..3 = the 4 pages' int8
+//                  centroid dims 0..63 against columns 0..3 (the heads' dims
+//                  0..63), rows 4..7 = dims 64..127 against columns 4..7;
 //   u . c_i        m16n8k16 f16, block-diagonal A = u of 4 pages x 4 heads
 //                  (split hi + lo f16 for ~22-bit precision), B = int8 c;
-// then a 4-lane shuffle log-sum-exp per (page, head).  Scores go to global
+// then a 4-lane shuffle log-sum-exp per (page, head), without a max shift
+// unless a row's sum leaves [2^-100, 2^100].  Scores go to global
 // memory; the selection reads them back to form Z_{b,h,g} and rank the pages.
 
 #include <cstdint>
@@ -50,14 +54,13 @@ __device__ __forceinline__ int request_full_pages(const ScoreParams& p, int b) {
 // row gid+8 = (page 2 + (gid>>2), head gid&3); identical on the 4 lanes of a
 // row quad.
 // qb: B operand (the group's 4 query heads, columns duplicated to 8), scaled
-// by 2^-e and, in the low-slot dims (k-step positions 0-7), by 16 more.
-// bias_v / bias_mu: the constant parts the biased code conversions add to
-// V^T q and q . mu for this lane's columns 2t and 2t+1 (removed by starting
-// the accumulators at -bias).
+// by 2^-e; qmb: the centroid's B operand (columns 0..3 dims 0..63, columns
+// 4..7 dims 64..127 of the same heads).  Codes enter the tensor cores as
+// their exact f16 values.
 template <int kStride>
-__device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t (&qb)[8][2], float pow2e,
-                                             const float (&bias_v)[2], const float (&bias_mu)[2],
-                                             int lane, float& s_r0, float& s_r1) {
+__device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t (&qb)[8][2],
+                                             const uint32_t (&qmb)[4][2], float pow2e, int lane,
+                                             float& s_r0, float& s_r1) {
   const int gid = lane >> 2, t = lane & 3;
   const float inv_sqrt_d = 0.08838834764831845f;
 
@@ -69,8 +72,8 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       v[pr][j] = *reinterpret_cast<const uint4*>(rec0 + (2 * pr + j) * kStride + gid * 64 + t * 16);
-    d1[pr][0] = d1[pr][2] = -bias_v[0];
-    d1[pr][1] = d1[pr][3] = -bias_v[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d1[pr][i] = 0.f;
   }
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -79,39 +82,44 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
       const uint32_t wa = w == 0 ? v[pr][0].x : w == 1 ? v[pr][0].y : w == 2 ? v[pr][0].z : v[pr][0].w;
       const uint32_t wb = w == 0 ? v[pr][1].x : w == 1 ? v[pr][1].y : w == 2 ? v[pr][1].z : v[pr][1].w;
       uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-      nib8_to_h2x4_biased(wa, a04, a15, a26, a37);
-      nib8_to_h2x4_biased(wb, b04, b15, b26, b37);
+      nib8_to_h2x4(wa, a04, a15, a26, a37);
+      nib8_to_h2x4(wb, b04, b15, b26, b37);
       mma_f16(d1[pr], a04, b04, a15, b15, qb[2 * w][0], qb[2 * w][1]);
       mma_f16(d1[pr], a26, b26, a37, b37, qb[2 * w + 1][0], qb[2 * w + 1][1]);
     }
   }
 
-  // ---- q . mu for the 4 pages: rows 0..3 of one m16 tile.  Rows 4..7
-  // repeat them (lanes gid >= 4 load page gid & 3) and are never read; rows
-  // 8..15 are zero.
-  float dmu[4] = {-bias_mu[0], -bias_mu[1], -bias_mu[0], -bias_mu[1]};
+  // ---- q . mu for the 4 pages in two halves of K: rows 0..3 hold the
+  // pages' centroid dims 0..63 against B columns 0..3 (dims 0..63 of the 4
+  // heads), rows 4..7 dims 64..127 against columns 4..7 (dims 64..127);
+  // cross terms are never read, rows 8..15 are zero.  Row p, column h plus
+  // row 4 + p, column 4 + h is q_h . mu_p: lane 4p + t adds lane 4p + t ^ 18.
+  float dmu[4] = {0.f, 0.f, 0.f, 0.f};
   {
-    const uint8_t* mp = rec0 + (gid & 3) * kStride + 512 + t * 32;
-    const uint4 m0 = *reinterpret_cast<const uint4*>(mp);
-    const uint4 m1 = *reinterpret_cast<const uint4*>(mp + 16);
-    const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const uint4 mq = *reinterpret_cast<const uint4*>(rec0 + (gid & 3) * kStride + 512 + t * 32 + (gid & 4) * 4);
+    const uint32_t mw[4] = {mq.x, mq.y, mq.z, mq.w};
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
+    for (int s = 0; s < 4; ++s) {
       uint32_t lo, hi;
-      i8x4_to_h2x2_biased(mw[s], lo, hi);
-      mma_f16(dmu, lo, 0u, hi, 0u, qb[s][0], qb[s][1]);
+      i8x4_to_h2x2(mw[s], lo, hi);
+      mma_f16(dmu, lo, 0u, hi, 0u, qmb[s][0], qmb[s][1]);
     }
+    dmu[0] += __shfl_xor_sync(0xffffffffu, dmu[0], 18);
+    dmu[1] += __shfl_xor_sync(0xffffffffu, dmu[1], 18);
   }
 
-  // ---- u -> f16 hi/lo, transposed into the block-diagonal A operand
+  // ---- u -> f16 hi/lo, transposed into the block-diagonal A operand.  The
+  // scalar steps from here on use explicitly rounded operations, so that the
+  // compiler cannot fuse a multiply into a later add for one page pair and not
+  // for the other: identical records then score bit-identically in any slot.
   uint32_t th[4], tl[4];
 #pragma unroll
   for (int pr = 0; pr < 2; ++pr) {
     const float f0 = *reinterpret_cast<const float*>(rec0 + (2 * pr) * kStride + 768) * inv_sqrt_d;
     const float f1 = *reinterpret_cast<const float*>(rec0 + (2 * pr + 1) * kStride + 768) * inv_sqrt_d;
     uint32_t h0, l0, h1, l1;
-    split_h2(d1[pr][0] * f0, d1[pr][1] * f0, h0, l0);
-    split_h2(d1[pr][2] * f1, d1[pr][3] * f1, h1, l1);
+    split_h2(__fmul_rn(d1[pr][0], f0), __fmul_rn(d1[pr][1], f0), h0, l0);
+    split_h2(__fmul_rn(d1[pr][2], f1), __fmul_rn(d1[pr][3], f1), h1, l1);
     th[2 * pr] = movmatrix_t(h0);
     tl[2 * pr] = movmatrix_t(l0);
     th[2 * pr + 1] = movmatrix_t(h1);
@@ -155,24 +163,45 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
   const float smu1 = *reinterpret_cast<const float*>(rec0 + pr1 * kStride + 772);
   const float sc_c0 = *reinterpret_cast<const float*>(rec0 + pr0 * kStride + 776) * (pow2e * kLog2e);
   const float sc_c1 = *reinterpret_cast<const float*>(rec0 + pr1 * kStride + 776) * (pow2e * kLog2e);
-  float x0[4] = {d2[0][0] * sc_c0, d2[0][1] * sc_c0, d2[1][0] * sc_c0, d2[1][1] * sc_c0};
-  float x1[4] = {d2[0][2] * sc_c1, d2[0][3] * sc_c1, d2[1][2] * sc_c1, d2[1][3] * sc_c1};
-  float m0 = fmaxf(fmaxf(x0[0], x0[1]), fmaxf(x0[2], x0[3]));
-  float m1 = fmaxf(fmaxf(x1[0], x1[1]), fmaxf(x1[2], x1[3]));
-  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+  float x0[4] = {__fmul_rn(d2[0][0], sc_c0), __fmul_rn(d2[0][1], sc_c0), __fmul_rn(d2[1][0], sc_c0),
+                 __fmul_rn(d2[1][1], sc_c0)};
+  float x1[4] = {__fmul_rn(d2[0][2], sc_c1), __fmul_rn(d2[0][3], sc_c1), __fmul_rn(d2[1][2], sc_c1),
+                 __fmul_rn(d2[1][3], sc_c1)};
+  // The sums of 2^x are taken without a max shift while both stay inside
+  // [2^-100, 2^100], where every term above 2^-126 is a normal float and the
+  // terms flushed to zero change the sum by less than 2^-22 of itself;
+  // otherwise the warp redoes them with each row's max taken out.
+  float m0 = 0.f, m1 = 0.f;
   float e0 = 0.f, e1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    e0 += fast_exp2(x0[i] - m0);
-    e1 += fast_exp2(x1[i] - m1);
+    e0 += fast_exp2(x0[i]);
+    e1 += fast_exp2(x1[i]);
   }
   e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
   e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
   e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
   e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
+  const bool in_range = e0 >= 0x1p-100f && e0 <= 0x1p100f && e1 >= 0x1p-100f && e1 <= 0x1p100f;
+  if (!__all_sync(0xffffffffu, in_range)) {
+    m0 = fmaxf(fmaxf(x0[0], x0[1]), fmaxf(x0[2], x0[3]));
+    m1 = fmaxf(fmaxf(x1[0], x1[1]), fmaxf(x1[2], x1[3]));
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    e0 = 0.f;
+    e1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e0 += fast_exp2(__fsub_rn(x0[i], m0));
+      e1 += fast_exp2(__fsub_rn(x1[i], m1));
+    }
+    e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
+    e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
+    e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
+    e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
+  }
 
   // ---- centroid term for the two rows, fetched from the mu tile's lanes
   const int hh = gid & 3;
@@ -184,12 +213,16 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
   const float b1 = __shfl_sync(0xffffffffu, dmu[1], src1);
   const float qmu0 = (hh & 1) ? a1 : a0;
   const float qmu1 = (hh & 1) ? b1 : b0;
-  s_r0 = qmu0 * smu0 * (pow2e * inv_sqrt_d) + (m0 + fast_log2(e0)) * kLn2;
-  s_r1 = qmu1 * smu1 * (pow2e * inv_sqrt_d) + (m1 + fast_log2(e1)) * kLn2;
+  const float cq = pow2e * inv_sqrt_d;
+  s_r0 = __fadd_rn(__fmul_rn(__fmul_rn(qmu0, smu0), cq), __fmul_rn(__fadd_rn(m0, fast_log2(e0)), kLn2));
+  s_r1 = __fadd_rn(__fmul_rn(__fmul_rn(qmu1, smu1), cq), __fmul_rn(__fadd_rn(m1, fast_log2(e1)), kLn2));
 }
 
 // kHcta: KV heads per CTA (1, 2, 4 or 8); a stage holds kPps pages of kHcta
 // heads each (32 records), warp w scores head w / kWph, pages 4 (w % kWph) ...
+// Two CTAs an SM: 18 warps put 5 on some SM sub-partition, whose 16,384
+// registers then allow at most 96 a thread; one register more halves the
+// occupancy.
 template <int kHcta>
 __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScoreParams p) {
   constexpr int kWph = 8 / kHcta;
@@ -300,8 +333,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
   uint32_t step = 0;
   int cur_b = -1, cur_h = -1;
   uint32_t qb[8][2];
+  uint32_t qmb[4][2];   // centroid B operand: columns 0..3 dims 0..63, columns 4..7 dims 64..127
   float pow2e = 1.f;
-  float bias_v[2] = {0.f, 0.f}, bias_mu[2] = {0.f, 0.f};
   bool ok = true;
 
   int it = it_begin;
@@ -319,9 +352,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 
     if (pg_begin < pg_end && (b != cur_b || h != cur_h)) {
       // B operand = the group's 4 query heads (duplicated into columns 4..7),
-      // pre-scaled by an exact power of two so every value fits f16, and by
-      // 16 more in the low-slot dims (positions 0-7 of each k-step), where
-      // the biased code conversions put a code at 1/16 of its value.
+      // pre-scaled by an exact power of two so every value fits f16.
       cur_b = b;
       cur_h = h;
       const __nv_bfloat16* qh = p.q + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup + (gid & 3)) * kHeadDim;
@@ -342,33 +373,20 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
       for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       int ex = 0;
       frexpf(amax, &ex);
-      const int e = ex > 11 ? ex - 11 : 0;   // 16 amax 2^-e < 2^15
+      const int e = ex > 15 ? ex - 15 : 0;   // amax 2^-e < 2^15
       pow2e = ldexpf(1.f, e);
       const float inv = ldexpf(1.f, -e);
-      float sum_lo = 0.f, sum_hi = 0.f;   // this lane's f16 operand values of column gid
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const __half2 lo = __floats2half2_rn(qv[s][0] * (16.f * inv), qv[s][1] * (16.f * inv));
+        const __half2 lo = __floats2half2_rn(qv[s][0] * inv, qv[s][1] * inv);
         const __half2 hi = __floats2half2_rn(qv[s][2] * inv, qv[s][3] * inv);
         qb[s][0] = *reinterpret_cast<const uint32_t*>(&lo);
         qb[s][1] = *reinterpret_cast<const uint32_t*>(&hi);
-        const float2 lf = __half22float2(lo), hf = __half22float2(hi);
-        sum_lo += lf.x + lf.y;
-        sum_hi += hf.x + hf.y;
       }
 #pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {   // column gid's sums over all 128 dims
-        sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, o);
-        sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, o);
-      }
-      // this lane's accumulator columns are 2t and 2t+1: their sums live on
-      // the lanes with gid == 2t and gid == 2t+1
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float lo = __shfl_sync(0xffffffffu, sum_lo, (2 * t + c) * 4);
-        const float hi = __shfl_sync(0xffffffffu, sum_hi, (2 * t + c) * 4);
-        bias_v[c] = 64.5f * lo + 72.f * hi;     // V: 64.5 + code/16 (low), 72 + code (high)
-        bias_mu[c] = 72.f * lo + 1152.f * hi;   // mu: 72 + code/16 (low), 1152 + code (high)
+      for (int s = 0; s < 4; ++s) {
+        qmb[s][0] = gid < 4 ? qb[s][0] : qb[s + 4][0];
+        qmb[s][1] = gid < 4 ? qb[s][1] : qb[s + 4][1];
       }
     }
 
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
         const uint32_t mask = live[s];
         const uint8_t* rec0 = stages + s * kScoreStageBytes + (sub * 4) * per_head_rec + hl * kRecord;
         float s_r0, s_r1;
-        score_group4<per_head_rec>(rec0, qb, pow2e, bias_v, bias_mu, lane, s_r0, s_r1);
+        score_group4<per_head_rec>(rec0, qb, qmb, pow2e, lane, s_r0, s_r1);
         const int slot0 = sub * 4 + (gid >> 2), slot1 = sub * 4 + 2 + (gid >> 2);
         const bool v0 = (mask >> slot0) & 1u, v1 = (mask >> slot1) & 1u;
         if (t == 0) {

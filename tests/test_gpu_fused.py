@@ -96,3 +96,58 @@ def test_fused_rejects_unsupported_budget():
                                      d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected,
                                      bufs.out, bufs.workspace)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kernel", ["select", "fused"])
+def test_selection_takes_lowest_index_copies_of_tied_rows(kernel):
+    """Score rows copied bit for bit across pages that straddle the budget
+    boundary: the copies have equal keys, and both selection kernels must
+    take the lowest-index ones (LOCKS summary §2: ties go to the lower page
+    index).  The scores are planted straight into the table, so the scorer's
+    own rounding plays no part."""
+    import oracle as O
+    from gpu_helpers import check_selection
+
+    w = _w(context=16 * 700 + 5, budget_tokens=16 * 40, seed=34)
+    run = Run(w)
+    H, bufs, d = run.H, run.bufs, run.d
+    n, k = run.lens[0] // 16, w.budget_pages
+    rng = np.random.default_rng(8)
+    tied = {}
+    for h in range(H):
+        base = (rng.normal(size=(n, 4)) * 2.0).astype(np.float32)
+        _, avg = O.select_pages(base.astype(np.float64), k)
+        order = np.argsort(-avg, kind="stable")
+        # copy one row to six lower-ranked pages; the copies move Z_g, so try
+        # source ranks from k - 3 upwards until the seven rows straddle the
+        # boundary in the oracle's own ranking
+        for r in range(k - 3, -1, -1):
+            table = base.copy()
+            src = order[r]
+            copies = rng.choice(order[r + 1:k + 40], size=6, replace=False)
+            table[copies] = table[src]
+            pages = np.sort(np.append(copies, src))
+            sel_or, _ = O.select_pages(table.astype(np.float64), k)
+            taken = np.intersect1d(sel_or, pages)
+            if 0 < taken.size < pages.size:
+                break
+        assert 0 < taken.size < pages.size, "the copies must straddle the boundary"
+        tied[h] = (pages, taken)
+        bufs.scores[0, h, :n] = torch.from_numpy(table).cuda()
+    sel = torch.full_like(bufs.selected, -1)
+    nsel = torch.full_like(bufs.n_selected, -1)
+    if kernel == "select":
+        L.locks_select(H, d["seq_lens"], w.max_pages, k, sel, nsel, bufs.workspace, scores=bufs.scores)
+    else:
+        out = torch.empty_like(bufs.out)
+        L.locks_select_sparse_decode(H, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"],
+                                     k, sel, nsel, out, bufs.workspace, scores=bufs.scores)
+    torch.cuda.synchronize()
+    assert L.locks_read_status(bufs.workspace) == 0
+    for h in range(H):
+        pages, taken = tied[h]
+        got = sel[0, h, :int(nsel[0, h])].cpu().numpy().astype(np.int64)
+        check_selection(got, bufs.scores[0, h, :n].double().cpu().numpy(), k)
+        got_tied = np.intersect1d(got, pages)
+        assert got_tied.tolist() == pages[:got_tied.size].tolist(), (h, pages, got_tied)
+        assert got_tied.tolist() == taken.tolist(), (h, got_tied, taken)

@@ -130,6 +130,31 @@ def test_pipeline_ragged_batch():
             check_unit(run, b, h)
 
 
+@pytest.mark.parametrize("q_scale", [30.0, 100.0, 300.0])
+def test_scores_with_huge_deviation_logits(q_scale):
+    """Queries scaled until a page's 16-token sum of 2^x passes 2^100 (x in
+    log2 units): those rows take the max-shifted log-sum-exp, the rest of the
+    warp's rows follow it, and every score must still match the oracle.
+    Selection is not compared here: the shares of most pages underflow in fp32
+    while fp64 keeps them apart."""
+    w = _w(context=16 * 200 + 3, seed=71)
+    d = W.generate(w, device="cuda")
+    d["q"] = (d["q"].float() * q_scale).to(torch.bfloat16)
+    run = Run(w, data=d)
+    assert run.status == 0
+    n = run.lens[0] // 16
+    past = 0
+    for h in range(w.num_kv_heads):
+        qg = run.q_group(0, h)
+        dq = O.dequantize(O.decode_records(run.records(0, h)))
+        s_ref = O.page_scores(qg, dq["mu"], dq["V"], dq["C"])
+        check_scores(run.gpu_scores(0, h), s_ref)
+        lse_dev = s_ref - dq["mu"] @ qg.T / math.sqrt(128)        # natural log of the deviation sum
+        past += int(np.sum(lse_dev * (1 / math.log(2)) > 100.0))
+    assert past > 0, "no row reached the max-shifted branch"
+    assert past < w.num_kv_heads * n * w.group, "every row reached it"
+
+
 def test_pipeline_exact_ties_go_to_lower_page_index():
     """Identical pages give identical records and scores: ties at the budget
     boundary must be broken by the lower page index."""
