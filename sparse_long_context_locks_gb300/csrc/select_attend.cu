@@ -166,46 +166,57 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   float* pub = reinterpret_cast<float*>(smem + 32768);               // [G][2 + 128] published
   attn_store_warp(st, wO + warp * kGroup * kHeadDim, wM + warp * kGroup, wL + warp * kGroup, lane);
   __syncthreads();
-  if (threadIdx.x < kHeadDim) {
-    const int d = threadIdx.x;
+  // warp 0, lane 4w + g: the factor exp2(m_{w,g} - M_g) of warp w's state for
+  // head g, M_g and the merged sum l_g; then every thread forms two of the
+  // CTA's G x 128 outputs from the 8 warps' states
+  __shared__ float fw[kFusedWarps][kGroup];
+  if (warp == 0) {
+    const int w = lane >> 2, g = lane & 3;
+    const float m = wM[w * kGroup + g];
+    float M = m;
 #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      float M = -INFINITY;
-      for (int w = 0; w < kFusedWarps; ++w) M = fmaxf(M, wM[w * kGroup + g]);
-      float Ls = 0.f, Os = 0.f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < kFusedWarps; ++w) {
-          const float f = fast_exp2(wM[w * kGroup + g] - M);
-          Ls += wL[w * kGroup + g] * f;
-          Os += wO[(w * kGroup + g) * kHeadDim + d] * f;
-        }
-      }
-      pub[g * (2 + kHeadDim) + 2 + d] = Os;
-      if (d == 0) {
-        pub[g * (2 + kHeadDim)] = M;
-        pub[g * (2 + kHeadDim) + 1] = Ls;
-      }
+    for (int o = 4; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float f = M == -INFINITY ? 0.f : fast_exp2(m - M);
+    fw[w][g] = f;
+    float l = wL[w * kGroup + g] * f;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (w == 0) {
+      pub[g * (2 + kHeadDim)] = M;
+      pub[g * (2 + kHeadDim) + 1] = l;
     }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kGroup * kHeadDim; i += blockDim.x) {
+    const int g = i / kHeadDim, d = i % kHeadDim;
+    float Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFusedWarps; ++w) Os += wO[(w * kGroup + g) * kHeadDim + d] * fw[w][g];
+    pub[g * (2 + kHeadDim) + 2 + d] = Os;
   }
   cluster.sync();   // every CTA's state is published
 
   // ---- merge the cluster: CTA `rank` finishes output dims [16 rank, 16 rank + 16)
   if (threadIdx.x < kGroup * 16) {
     const int g = threadIdx.x >> 4, d = 16 * rank + (threadIdx.x & 15);
-    float mr[kSelCluster], M = -INFINITY;
+    // every remote load is issued before any of them is used
+    float mr[kSelCluster], lr[kSelCluster], orr[kSelCluster], M = -INFINITY;
 #pragma unroll
     for (int r = 0; r < kSelCluster; ++r) {
-      mr[r] = *cluster.map_shared_rank(&pub[g * (2 + kHeadDim)], r);
-      M = fmaxf(M, mr[r]);
+      const float* rp = cluster.map_shared_rank(&pub[g * (2 + kHeadDim)], r);
+      mr[r] = rp[0];
+      lr[r] = rp[1];
+      orr[r] = rp[2 + d];
     }
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) M = fmaxf(M, mr[r]);
     float Ls = 0.f, Os = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int r = 0; r < kSelCluster; ++r) {
-        const float* rp = cluster.map_shared_rank(&pub[g * (2 + kHeadDim)], r);
         const float f = fast_exp2(mr[r] - M);
-        Ls += rp[1] * f;
-        Os += rp[2 + d] * f;
+        Ls += lr[r] * f;
+        Os += orr[r] * f;
       }
     }
     p.out[((int64_t)b * p.sel.H_kv * kGroup + (int64_t)h * kGroup + g) * kHeadDim + d] = Ls > 0.f ? Os / Ls : 0.f;
