@@ -13,7 +13,7 @@ import torch
 import oracle as O
 from sparse_long_context_locks_gb300 import workload as W
 
-from gpu_helpers import Run, check_records, check_unit
+from gpu_helpers import Run, check_fused_unit, check_records, check_unit
 
 pytestmark = pytest.mark.gpu
 
@@ -82,4 +82,23 @@ def test_batch64_256k_sampled_requests(regime):
         for h in range(8):
             check_unit(run, b, h, check_scores_too=(h % 4 == 0))
     _check_build_sample(run, 17, 2, 512, rng)
+    _free(run)
+
+
+def test_maximum_context_and_budget():
+    """The largest request the fused step accepts: 131,072 pages (2,097,151
+    tokens, so a 15-token tail), each selecting CTA's 16,384 keys and block ids
+    filling its 128 KB ring, and a 2,047-page budget (32 items for each of the
+    cluster's 64 warps with the tail).  Scores of one head against the oracle,
+    every head's selection from its scores and the step's attention."""
+    w = W.Workload("max_2m", batch=1, context=16 * 131072 - 1, num_kv_heads=8, group=4,
+                   budget_tokens=16 * 2047, carriers_per_head=16, seed=77)
+    assert w.max_pages == 131072 and w.budget_pages == 2047
+    run = Run(w, step=True)
+    assert run.status == 0
+    rng = np.random.default_rng(3)
+    for h in range(8):
+        check_unit(run, 0, h, check_scores_too=(h == 3))
+        check_fused_unit(run, 0, h, which="step")
+    _check_build_sample(run, 0, 1, 1024, rng)
     _free(run)
