@@ -357,12 +357,9 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 }
 
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DynSmemAttr smem_attr;
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(build_kernel), kBuildSmem, smem_attr);
+  if (e != cudaSuccess) return e;
   const int64_t page_heads = (int64_t)p.n_build * p.H_kv;
   const int64_t grid = (page_heads + 2 * kBuildWarps - 1) / (2 * kBuildWarps);
   if (grid == 0) return cudaSuccess;

@@ -7,6 +7,7 @@
 // LOCKS_FLAG_TIMEOUT in the status word and reports failure to the caller.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -16,6 +17,30 @@
 #include "../../include/locks.h"
 
 namespace locks {
+
+// Host side: the dynamic shared memory a kernel may use is an attribute of the
+// kernel on the current device.  DynSmemAttr records, per device, the largest
+// size already set, so a launcher sets it once per device and size (and again
+// when a larger size is needed); safe to call from several host threads.
+constexpr int kMaxDevices = 64;
+struct DynSmemAttr {
+  std::atomic<size_t> set[kMaxDevices] = {};
+};
+inline cudaError_t ensure_dyn_smem(const void* kernel, size_t bytes, DynSmemAttr& rec) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  size_t cur = rec.set[dev].load(std::memory_order_acquire);
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  while (cur < bytes && !rec.set[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+  }
+  return cudaSuccess;
+}
+
 
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;

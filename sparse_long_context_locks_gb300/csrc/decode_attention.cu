@@ -294,12 +294,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DynSmemAttr smem_attr;
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(attn_kernel), kAttnSmem, smem_attr);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.splits, p.batch * p.H_kv);
   attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(tmk, tmv, p);
   return cudaGetLastError();

@@ -34,7 +34,6 @@ using namespace locks;
 
 constexpr size_t kScratchBytes = size_t(8) << 20;   // 8 MiB per device
 constexpr size_t kHeaderBytes = 256;                 // status word
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 

@@ -435,13 +435,9 @@ namespace locks {
 
 template <int kHcta>
 cudaError_t launch_score_t(const ScoreParams& p, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(score_kernel<kHcta>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static DynSmemAttr smem_attr;
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(score_kernel<kHcta>), kScoreSmem, smem_attr);
+  if (e != cudaSuccess) return e;
   score_kernel<kHcta><<<grid, kScoreThreads, kScoreSmem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -458,12 +454,9 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
 
 cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream) {
   const size_t dyn = select_smem_bytes(p.max_pages, p.budget);
-  static size_t attr_bytes = 0;
-  if (dyn > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-    if (e != cudaSuccess) return e;
-    attr_bytes = dyn;
-  }
+  static DynSmemAttr smem_attr;
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel), dyn, smem_attr);
+  if (e != cudaSuccess) return e;
   dim3 grid(kSelCluster, units);
   select_kernel<<<grid, kSelThreads, dyn, stream>>>(p);
   return cudaGetLastError();

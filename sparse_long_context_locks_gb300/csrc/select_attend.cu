@@ -227,12 +227,9 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 cudaError_t launch_select_attend(const CUtensorMap& tmk, const CUtensorMap& tmv, const FusedParams& p,
                                  int units, cudaStream_t stream) {
   const size_t dyn = fused_smem_bytes(p.sel.max_pages, p.sel.budget);
-  static size_t attr_bytes = 0;
-  if (dyn > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(select_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
-    if (e != cudaSuccess) return e;
-    attr_bytes = dyn;
-  }
+  static DynSmemAttr smem_attr;
+  const cudaError_t ea = ensure_dyn_smem(reinterpret_cast<const void*>(select_attend_kernel), dyn, smem_attr);
+  if (ea != cudaSuccess) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kSelCluster, units, 1);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
