@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
 FLAG_BAD_BLOCK, FLAG_BAD_SEQLEN, FLAG_TIMEOUT, FLAG_BAD_SELECT = 1, 2, 4, 8
 
 HEAD_DIM, PAGE_SIZE, RANK, GROUP = 128, 16, 8, 4
+RECORD_BYTES = 784   # one page-head summary record
 
 
 class LocksError(RuntimeError):
@@ -140,8 +141,57 @@ def _nbytes(t) -> int:
     return 0 if t is None else t.numel() * t.element_size()
 
 
+# ------------------------------------------------------------------ argument checks
+# The C ABI receives bare pointers, so the layouts it assumes (include/locks.h)
+# are checked here, before any pointer is passed: a contiguous CUDA tensor of
+# the stated dtype and shape.  A mismatch raises ValueError.
+def _req(t, name: str, dtype: str, shape=None, optional: bool = False) -> None:
+    """shape: a tuple of sizes, None for a free axis (its rank is checked)."""
+    import torch
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    want = getattr(torch, dtype)
+    if t.dtype != want:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None:
+        if t.dim() != len(shape) or any(n is not None and t.shape[i] != n for i, n in enumerate(shape)):
+            want_s = "[" + ", ".join("*" if n is None else str(n) for n in shape) + "]"
+            raise ValueError(f"{name} must have shape {want_s}, got {list(t.shape)}")
+
+
+def _req_cache(t, name: str, H: int) -> None:
+    _req(t, name, "bfloat16", (None, H, PAGE_SIZE, HEAD_DIM))
+
+
+def _req_step(H, q, block_table, seq_lens) -> tuple:
+    """q [batch, H*G, 128] bf16; block_table [batch, max_pages] int32;
+    seq_lens [batch] int32.  Returns (batch, max_pages)."""
+    _req(block_table, "block_table", "int32", (None, None))
+    B, MP = block_table.shape
+    _req(seq_lens, "seq_lens", "int32", (B,))
+    if q is not None:
+        _req(q, "q", "bfloat16", (B, H * GROUP, HEAD_DIM))
+    return B, MP
+
+
+def _req_selection(H, B, budget_pages, selected, n_selected) -> None:
+    _req(n_selected, "n_selected", "int32", (B, H))
+    _req(selected, "selected", "int32", (B, H, budget_pages) if budget_pages > 0 else None,
+         optional=budget_pages == 0)
+
+
 # ------------------------------------------------------------------ calls
 def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace=None, stream=None):
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(block_ids, "block_ids", "int32", (None,))
+    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, RECORD_BYTES))
+    _req(workspace, "workspace", "uint8", optional=True)
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_build_summaries(
         ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), block_ids.numel(),
@@ -154,6 +204,11 @@ def locks_build_pending(num_kv_heads, k_cache, block_ids, n_pending, summaries, 
     """Build the records of block_ids[0, n_pending[0]) (n_pending: a device
     int32 tensor, read by the kernel); block_ids holds room for the most pages
     any step can finalise."""
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(block_ids, "block_ids", "int32", (None,))
+    _req(n_pending, "n_pending", "int32", (None,))
+    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, RECORD_BYTES))
+    _req(workspace, "workspace", "uint8", optional=True)
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_build_pending(
         ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), _ptr(n_pending),
@@ -163,6 +218,10 @@ def locks_build_pending(num_kv_heads, k_cache, block_ids, n_pending, summaries, 
 
 def locks_score(num_kv_heads, q, summaries, block_table, seq_lens, workspace, scores=None,
                 stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_score(
         ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
@@ -172,6 +231,11 @@ def locks_score(num_kv_heads, q, summaries, block_table, seq_lens, workspace, sc
 
 def locks_select(num_kv_heads, seq_lens, max_pages, budget_pages, selected, n_selected, workspace,
                  scores=None, stream=None):
+    _req(seq_lens, "seq_lens", "int32", (None,))
+    B = seq_lens.shape[0]
+    _req(scores, "scores", "float32", (B, num_kv_heads, max_pages, GROUP), optional=True)
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_select(
         ctypes.byref(cfg), _ptr(seq_lens), seq_lens.shape[0], max_pages, budget_pages, _ptr(scores),
@@ -181,6 +245,11 @@ def locks_select(num_kv_heads, seq_lens, max_pages, budget_pages, selected, n_se
 
 def locks_score_select(num_kv_heads, q, summaries, block_table, seq_lens, budget_pages, selected,
                        n_selected, workspace, scores=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_score_select(
         ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
@@ -191,6 +260,12 @@ def locks_score_select(num_kv_heads, q, summaries, block_table, seq_lens, budget
 
 def locks_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, selected,
                         n_selected, budget_pages, out, workspace, sm_scale=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_sparse_decode(
@@ -203,6 +278,13 @@ def locks_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens
 def locks_select_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens,
                                budget_pages, selected, n_selected, out, workspace, scores=None,
                                sm_scale=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_select_sparse_decode(
@@ -215,6 +297,14 @@ def locks_select_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, s
 def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table, seq_lens,
                       budget_pages, selected, n_selected, out, workspace, scores=None,
                       sm_scale=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_decode_step(
@@ -227,6 +317,11 @@ def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table,
 
 def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, out, workspace,
                        sm_scale=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_dense_decode(
@@ -239,6 +334,11 @@ def locks_sparse_decode_noalloc(num_kv_heads, q, k_cache, v_cache, block_table, 
                                 n_selected, budget_pages, out, sm_scale=None, stream=None):
     """locks_sparse_decode for callers that cannot allocate: the library's own
     fixed device scratch replaces the workspace (see include/locks.h)."""
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_sparse_decode_noalloc(
