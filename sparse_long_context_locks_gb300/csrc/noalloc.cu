@@ -21,6 +21,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -105,13 +106,13 @@ extern "C" locks_status locks_sparse_decode_noalloc(
     return LOCKS_ERR_INVALID_ARG;
   if (num_blocks * H * kPage >= (int64_t)1 << 31) return LOCKS_ERR_UNSUPPORTED;
 
-  // same split rule as the workspace entry point: ~8 waves of resident CTAs,
+  // same split rule as the workspace entry point: one wave of resident CTAs,
   // at least one item per warp
   const int64_t units = (int64_t)batch * H;
   const int64_t items = (int64_t)budget_pages + 1;
   const int64_t by_items = (items + 3) / 4;
-  const int64_t want = (8 * (int64_t)kTargetCtas + units - 1) / units;
-  const int splits = (int)(by_items < want ? (by_items > 0 ? by_items : 1) : (want > 0 ? want : 1));
+  const int64_t want = units > 0 ? kTargetCtas / units : 1;
+  const int splits = (int)std::max<int64_t>(1, std::min(by_items, want));
   const int ips = (int)((items + splits - 1) / splits);
   const size_t tickets_bytes = ((size_t)units * sizeof(uint32_t) + 255) / 256 * 256;
   const size_t need = kHeaderBytes + tickets_bytes + (size_t)units * splits * kGroup * (2 + kHeadDim) * sizeof(float);
