@@ -172,9 +172,10 @@ locks_status locks_score(const locks_cfg *cfg, const void *q, const void *summar
  * the min(budget_pages, n_b) largest entries (lower page index on ties) are
  * written to selected[b][h][...] in ascending page order and their count to
  * n_selected[b][h].  `scores` must be what locks_score was given.  One
- * cluster of 8 CTAs per (b, h) computes Z from the scores and selects by an
- * exact cluster-wide radix select.  Needs max_pages <= 131072, else
- * LOCKS_ERR_UNSUPPORTED. */
+ * thread-block cluster per (b, h) -- 2 CTAs, or 4 or 8 when a CTA's slice of
+ * max_pages would exceed 16,384 pages -- computes Z from the scores and
+ * selects by an exact cluster-wide radix select.  Needs max_pages <= 131072,
+ * else LOCKS_ERR_UNSUPPORTED. */
 locks_status locks_select(const locks_cfg *cfg, const int32_t *seq_lens, int32_t batch,
                           int32_t max_pages, int32_t budget_pages, const float *scores,
                           int32_t *selected, int32_t *n_selected,

@@ -106,6 +106,20 @@ int num_sms() {
   return cached[dev];
 }
 
+// CTAs per (request, KV head) in the selection kernel: the smallest power of
+// two from 2 whose slices fit the per-CTA key limit and shared memory.  Its
+// clusters are latency-bound (a handful of cluster barriers and remote reads
+// each), and on a GB300 two CTAs with four times the keys beat eight: batch
+// 16 x 32K selects in 14.5 us (24.7 with 8), batch 64 x 256K in 85.6 us
+// (116.5 with 8).  (A single CTA is slower again: 18.5 and 92.3 us.)
+int select_cluster(int max_pages, int budget) {
+  int c = 2;
+  while (c < kSelCluster && ((max_pages + c - 1) / c > kFusedMaxKeysPerCta ||
+                             select_smem_bytes(max_pages, budget, c) > (size_t)kSmemLimit))
+    c *= 2;
+  return c;
+}
+
 #define LOCKS_CHECK_PTR(p) \
   do {                     \
     if ((p) == nullptr || !aligned16(p)) return LOCKS_ERR_INVALID_ARG; \
@@ -362,7 +376,9 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
   SelectParams p{};
   fill_select(p, pl, cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected, workspace);
-  return from_cuda(launch_select(p, batch * cfg->num_kv_heads, reinterpret_cast<cudaStream_t>(stream)));
+  const int units = batch * cfg->num_kv_heads;
+  return from_cuda(launch_select(p, units, select_cluster(max_pages, budget_pages),
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 locks_status locks_select_sparse_decode(const locks_cfg* cfg, const void* q, const void* k_cache,

@@ -9,8 +9,8 @@
 // query heads into one table; the k largest entries (lower page index on
 // ties) are attended.
 //
-// One cluster of kSelCluster CTAs per (request, KV head); CTA r owns pages
-// [n r / C, n (r + 1) / C).
+// One cluster of C CTAs per (request, KV head) (C a power of two, at most 8);
+// CTA r owns pages [n r / C, n (r + 1) / C).
 //   1. Z_g: each CTA folds its slice's scores into a (max, sum) pair per head
 //      and publishes it in shared memory; after a cluster barrier every CTA
 //      combines the C pairs, read through distributed shared memory.
@@ -142,6 +142,7 @@ struct SelScratch {
 // of the cluster must call it.  Writes `selected` and `n_selected`; ends with
 // a cluster barrier after which rank 0's out_blk[0, kk) may be read through
 // distributed shared memory.
+template <int C>
 static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScratch& sc) {
   __shared__ __align__(16) int hist0[1 << 11];
   __shared__ __align__(16) int hist1[1 << 10];
@@ -151,7 +152,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   __shared__ float red_m[kSelWarps][kGroup], red_s[kSelWarps][kGroup];
   __shared__ float zl[kGroup];
   __shared__ int scan_buf[32];
-  __shared__ int bnd_cnt[kSelCluster];         // per-CTA count in the boundary bin
+  __shared__ int bnd_cnt[C];         // per-CTA count in the boundary bin
   __shared__ int s_bin, s_above, s_cutoff, s_cnt;
   __shared__ int chunk_base[kSelMaxChunks];
 
@@ -177,8 +178,8 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   res.tail = L % kPage;
   const int kk = min(p.budget, n);
   res.kk = kk;
-  const int j0 = (int)(((long long)n * rank) / kSelCluster);
-  const int j1 = (int)(((long long)n * (rank + 1)) / kSelCluster);
+  const int j0 = (int)(((long long)n * rank) / C);
+  const int j1 = (int)(((long long)n * (rank + 1)) / C);
   const int len = j1 - j0;
   if (n <= p.budget || kk == 0) {   // every full page is selected (or none is)
     if (kk > 0) {
@@ -249,13 +250,13 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   }
   cluster.sync();   // every CTA's (max, sum) pairs and cleared histograms are visible
   if (tid < kGroup) {
-    float2 pr[kSelCluster];   // issue every remote load before merging
+    float2 pr[C];   // issue every remote load before merging
 #pragma unroll
-    for (int r = 0; r < kSelCluster; ++r)
+    for (int r = 0; r < C; ++r)
       pr[r] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(&lse_pub[tid][0], r));
     float mx = -INFINITY, sv = 0.f;
 #pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) lse2_merge(mx, sv, pr[r].x, pr[r].y);
+    for (int r = 0; r < C; ++r) lse2_merge(mx, sv, pr[r].x, pr[r].y);
     zl[tid] = mx + fast_log2(sv);   // log2 Z_g
   }
   __syncthreads();
@@ -298,13 +299,13 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   // level 0: walk the bins top-down from the highest occupied one, 32 bins a
   // round; thread t reads CTA (t % 8)'s count of bin top - t / 8
   {
-    if (tid < kSelCluster) scan_buf[tid] = *cluster.map_shared_rank(&s_hmax, tid);
+    if (tid < C) scan_buf[tid] = *cluster.map_shared_rank(&s_hmax, tid);
     __syncthreads();
     int hi = -1;
 #pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) hi = max(hi, scan_buf[r]);
+    for (int r = 0; r < C; ++r) hi = max(hi, scan_buf[r]);
     __syncthreads();
-    const int r_of = tid % kSelCluster;
+    const int r_of = tid % C;
     int add_mine = 0, add_before = 0;
     int carry = 0;   // keys in the bins above this round
     bool found = false;
@@ -312,17 +313,17 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       s_bin = 0;
       s_above = 0;
     }
-    for (int top = hi; top >= 0 && !found; top -= kSelThreads / kSelCluster) {
-      const int bin = top - tid / kSelCluster;
+    for (int top = hi; top >= 0 && !found; top -= kSelThreads / C) {
+      const int bin = top - tid / C;
       const int v = bin >= 0 ? *cluster.map_shared_rank(&hist0[bin], r_of) : 0;
       // bin total over the 8 CTAs: lanes 8k..8k+7 hold one bin
       int tot = v;
 #pragma unroll
-      for (int o = 1; o < kSelCluster; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      for (int o = 1; o < C; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
       int round_total;
       const int above = carry + block_exclusive_scan(r_of == 0 ? tot : 0, scan_buf, round_total);
       // `above` on lane r_of == 0 of each bin; share it with the bin's lanes
-      const int above_bin = __shfl_sync(0xffffffffu, above, lane & ~(kSelCluster - 1));
+      const int above_bin = __shfl_sync(0xffffffffu, above, lane & ~(C - 1));
       const bool is_bnd = bin >= 0 && above_bin < need && above_bin + tot >= need;
       if (is_bnd) {
         bnd_cnt[r_of] = v;
@@ -352,7 +353,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   }
   int in_bin = 0, lower = 0;
 #pragma unroll
-  for (int r = 0; r < kSelCluster; ++r) {
+  for (int r = 0; r < C; ++r) {
     in_bin += bnd_cnt[r];
     if (r < rank) lower += bnd_cnt[r];
   }
@@ -431,9 +432,9 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       constexpr int per = 4;
       const int top = (1 << 10) - 1 - per * tid;
       const int lo_bin = top - per + 1;
-      int v[kSelCluster][per];
+      int v[C][per];
 #pragma unroll
-      for (int r = 0; r < kSelCluster; ++r) {   // every remote load first
+      for (int r = 0; r < C; ++r) {   // every remote load first
         const int4 q = *reinterpret_cast<const int4*>(cluster.map_shared_rank(hist, r) + lo_bin);
         v[r][0] = q.x;
         v[r][1] = q.y;
@@ -442,7 +443,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       }
       int c[per] = {0, 0, 0, 0};
 #pragma unroll
-      for (int r = 0; r < kSelCluster; ++r)
+      for (int r = 0; r < C; ++r)
 #pragma unroll
         for (int i = 0; i < per; ++i) c[i] += v[r][i];
       const int cnt_all = c[0] + c[1] + c[2] + c[3];
@@ -466,7 +467,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       const int bin = s_bin;
       int add_mine = 0, add_before = 0;
 #pragma unroll
-      for (int r = 0; r < kSelCluster; ++r)
+      for (int r = 0; r < C; ++r)
 #pragma unroll
         for (int i = 0; i < per; ++i) {
           if (lo_bin + i > bin) {
@@ -482,7 +483,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       need -= s_above;
       int inb = 0, low = 0;
 #pragma unroll
-      for (int r = 0; r < kSelCluster; ++r) {
+      for (int r = 0; r < C; ++r) {
         inb += bnd_cnt[r];
         if (r < rank) low += bnd_cnt[r];
       }

@@ -55,8 +55,8 @@ constexpr int kSmemLimit = 200 * 1024;     // dynamic shared memory we allow a C
 
 // Dynamic shared memory of the selection kernel: slice keys and the selected
 // list (rank 0).
-__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget) {
-  const int slice_cap = (max_pages + kSelCluster - 1) / kSelCluster;
+__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget, int cluster = kSelCluster) {
+  const int slice_cap = (max_pages + cluster - 1) / cluster;
   return 4 * ((size_t)slice_cap + (size_t)budget + 4);
 }
 

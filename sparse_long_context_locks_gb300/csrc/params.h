@@ -76,7 +76,8 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_select_attend(const CUtensorMap& tmk, const CUtensorMap& tmv, const FusedParams& p,
                                  int units, cudaStream_t stream);
 size_t fused_smem_bytes(int max_pages, int budget);
-cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream);
+// cluster: CTAs per (request, KV head): 1, 2, 4 or 8
+cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream);
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream);
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream);

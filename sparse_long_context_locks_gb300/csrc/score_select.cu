@@ -416,16 +416,17 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // ---------------------------------------------------------------- select
 
 
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 4)
-    select_kernel(const SelectParams p) {
+// One cluster of C CTAs per (request, KV head).
+template <int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) select_kernel(const SelectParams p) {
   // [slice keys][selected list]
   extern __shared__ __align__(16) uint32_t sel_dyn[];
-  const int slice_cap = (p.max_pages + kSelCluster - 1) / kSelCluster;
+  const int slice_cap = (p.max_pages + C - 1) / C;
   SelScratch sc;
   sc.keys_s = sel_dyn;
   sc.bt_slice = nullptr;
   sc.out_blk = reinterpret_cast<int*>(sel_dyn + slice_cap);
-  cluster_select(p, sc);
+  cluster_select<C>(p, sc);
 }
 
 }  // namespace locks
@@ -452,14 +453,25 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
   }
 }
 
-cudaError_t launch_select(const SelectParams& p, int units, cudaStream_t stream) {
-  const size_t dyn = select_smem_bytes(p.max_pages, p.budget);
+template <int C>
+cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t stream) {
+  const size_t dyn = select_smem_bytes(p.max_pages, p.budget, C);
   static DynSmemAttr smem_attr;
-  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel), dyn, smem_attr);
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C>), dyn, smem_attr);
   if (e != cudaSuccess) return e;
-  dim3 grid(kSelCluster, units);
-  select_kernel<<<grid, kSelThreads, dyn, stream>>>(p);
+  dim3 grid(C, units);
+  select_kernel<C><<<grid, kSelThreads, dyn, stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream) {
+  switch (cluster) {
+    case 8: return launch_select_c<8>(p, units, stream);
+    case 4: return launch_select_c<4>(p, units, stream);
+    case 2: return launch_select_c<2>(p, units, stream);
+    case 1: return launch_select_c<1>(p, units, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace locks
