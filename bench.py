@@ -397,7 +397,9 @@ def main():
     # locks_decode_step runs the fused cluster kernel when every (request, KV
     # head) cluster of 8 CTAs fits on the GPU at once, else selection + split-K
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
-    fused_path = B * H * 8 <= n_sms
+    # the library's rule: every (request, KV head) cluster of 8 CTAs resident
+    # at once, and at most 32,768 pages of context
+    fused_path = B * H * 8 <= n_sms and w.max_pages <= 32768
     launches_per_step = 2 if fused_path else 3
     config["step_path"] = "score + fused select/attend" if fused_path else "score + select + split-K attend"
 

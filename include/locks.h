@@ -172,9 +172,10 @@ locks_status locks_score(const locks_cfg *cfg, const void *q, const void *summar
  * the min(budget_pages, n_b) largest entries (lower page index on ties) are
  * written to selected[b][h][...] in ascending page order and their count to
  * n_selected[b][h].  `scores` must be what locks_score was given.  One
- * thread-block cluster per (b, h) -- 2 CTAs, or 4 or 8 when a CTA's slice of
- * max_pages would exceed 16,384 pages -- computes Z from the scores and
- * selects by an exact cluster-wide radix select.  Needs max_pages <= 131072,
+ * thread-block cluster per (b, h) -- 8 CTAs when all of them fit on the GPU
+ * at once, else 2 (or 4 or 8 when a CTA's slice of max_pages would exceed
+ * 16,384 pages) -- computes Z from the scores and selects by an exact
+ * cluster-wide radix select.  Needs max_pages <= 131072,
  * else LOCKS_ERR_UNSUPPORTED. */
 locks_status locks_select(const locks_cfg *cfg, const int32_t *seq_lens, int32_t batch,
                           int32_t max_pages, int32_t budget_pages, const float *scores,
@@ -223,10 +224,11 @@ locks_status locks_select_sparse_decode(const locks_cfg *cfg, const void *q, con
 
 /* One whole LOCKS decode step for a batch: locks_score, then either
  * locks_select_sparse_decode (when batch * num_kv_heads clusters of 8 CTAs
- * fit on the GPU at once; the second kernel is a programmatic dependent of
- * the first) or locks_select followed by locks_sparse_decode (larger
- * batches, where the cluster kernel would run in many waves).  Same results
- * either way; same limits as the fused call. */
+ * fit on the GPU at once and max_pages <= 32768) or locks_select followed by
+ * locks_sparse_decode (larger batches, where the cluster kernel would run in
+ * many waves, and longer contexts, where its long per-CTA slices cost more).
+ * Each kernel after the first is a programmatic dependent of the one before
+ * it.  Same results either way; same limits as the fused call. */
 locks_status locks_decode_step(const locks_cfg *cfg, const void *q, const void *summaries,
                                const void *k_cache, const void *v_cache, int64_t num_blocks,
                                const int32_t *block_table, const int32_t *seq_lens, int32_t batch,

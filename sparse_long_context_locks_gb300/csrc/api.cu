@@ -47,6 +47,9 @@ bool cfg_supported(const locks_cfg* c) {
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Longest context (in pages) for which locks_decode_step takes the fused kernel.
+constexpr int kFusedStepMaxPages = 32768;
+
 int pick_splits(int units, int max_items) {
   // aim for ~8 waves of resident CTAs, at least 4 items (one per warp) each
   const int by_items = max(1, ceil_div(max_items, 4));
@@ -106,13 +109,15 @@ int num_sms() {
   return cached[dev];
 }
 
-// CTAs per (request, KV head) in the selection kernel: the smallest power of
-// two from 2 whose slices fit the per-CTA key limit and shared memory.  Its
-// clusters are latency-bound (a handful of cluster barriers and remote reads
-// each), and on a GB300 two CTAs with four times the keys beat eight: batch
-// 16 x 32K selects in 14.5 us (24.7 with 8), batch 64 x 256K in 85.6 us
-// (116.5 with 8).  (A single CTA is slower again: 18.5 and 92.3 us.)
-int select_cluster(int max_pages, int budget) {
+// CTAs per (request, KV head) in the selection kernel (8, 4 or 2).  Its
+// clusters are latency-bound.  When every 8-CTA cluster of the batch is
+// resident at once (4 CTAs an SM), 8 keeps each CTA's slice shortest: one
+// request at 128K selects in ~15 us (26.6 with 2).  With more units the
+// waves cost more than the slices save, and the smallest cluster whose slices
+// fit the per-CTA key limit is best: batch 16 x 32K selects in 14.5 us with 2
+// (16.4 with 4, 24.7 with 8), batch 64 x 256K in 85.6 us (116.5 with 8).
+int select_cluster(int units, int max_pages, int budget) {
+  if ((int64_t)units * kSelCluster <= 4 * (int64_t)num_sms()) return kSelCluster;
   int c = 2;
   while (c < kSelCluster && ((max_pages + c - 1) / c > kFusedMaxKeysPerCta ||
                              select_smem_bytes(max_pages, budget, c) > (size_t)kSmemLimit))
@@ -377,7 +382,7 @@ locks_status locks_select(const locks_cfg* cfg, const int32_t* seq_lens, int32_t
   SelectParams p{};
   fill_select(p, pl, cfg, seq_lens, batch, max_pages, budget_pages, scores, selected, n_selected, workspace);
   const int units = batch * cfg->num_kv_heads;
-  return from_cuda(launch_select(p, units, select_cluster(max_pages, budget_pages),
+  return from_cuda(launch_select(p, units, select_cluster(units, max_pages, budget_pages),
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -445,8 +450,12 @@ locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* 
   // One cluster per (request, KV head): when they all fit on the GPU at once
   // the fused kernel keeps the selection on chip; with more units its
   // latency-bound clusters would run in many waves, so the selection kernel
-  // (small CTAs, many resident per SM) and the split-K attention run instead.
-  if ((int64_t)batch * cfg->num_kv_heads * kSelCluster <= num_sms())
+  // (small CTAs, many resident per SM) and the split-K attention run instead,
+  // each a programmatic dependent of the kernel before it.  Past 32,768 pages
+  // a fused CTA's slice (4,096+ keys) and its attention share make the
+  // separate path faster too: one request at 1M tokens takes 133.3 us that
+  // way against 137.7 us fused (equal at 512K, fused ahead below).
+  if ((int64_t)batch * cfg->num_kv_heads * kSelCluster <= num_sms() && max_pages <= kFusedStepMaxPages)
     return locks_select_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, batch, max_pages,
                                       budget_pages, scores, selected, n_selected, sm_scale, out, workspace,
                                       workspace_bytes, stream);

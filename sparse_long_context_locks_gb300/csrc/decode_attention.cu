@@ -92,14 +92,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int unit = blockIdx.y, split = blockIdx.x;
   const int b = unit / p.H_kv, h = unit % p.H_kv;
 
-  int n, tail, nsel, items;
-  unit_items(p, b, h, n, tail, nsel, items);
-  const int r0 = min(items, split * p.items_per_split);
-  const int r1 = min(items, r0 + p.items_per_split);
-  // this warp's items: r0 + warp, r0 + warp + 4, ...
-  const int my_first = r0 + warp;
-  const int my_count = my_first < r1 ? (r1 - my_first + kAttnWarps - 1) / kAttnWarps : 0;
-
   uint64_t* mybar = bars + warp * kAttnStages;
   const uint32_t ring = smem_u32(smem) + warp * kAttnStages * kStageBytes;
   uint8_t* ring_ptr = smem + warp * kAttnStages * kStageBytes;
@@ -110,6 +102,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     prefetch_tmap(&tmv);
   }
   __syncwarp();
+  // launched as a programmatic dependent of the selection: its lists are
+  // visible from here on
+  griddep_wait();
+
+  int n, tail, nsel, items;
+  unit_items(p, b, h, n, tail, nsel, items);
+  const int r0 = min(items, split * p.items_per_split);
+  const int r1 = min(items, r0 + p.items_per_split);
+  // this warp's items: r0 + warp, r0 + warp + 4, ...
+  const int my_first = r0 + warp;
+  const int my_count = my_first < r1 ? (r1 - my_first + kAttnWarps - 1) / kAttnWarps : 0;
 
   // Item metadata windows: lane l of `cur` describes issue index base + l,
   // `nxt` the 32 after it (loaded one window ahead so refills never wait).
@@ -297,8 +300,18 @@ cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const At
   static DynSmemAttr smem_attr;
   const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(attn_kernel), kAttnSmem, smem_attr);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.splits, p.batch * p.H_kv);
-  attn_kernel<<<grid, kAttnThreads, kAttnSmem, stream>>>(tmk, tmv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.batch * p.H_kv, 1);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, attn_kernel, tmk, tmv, p);
+  if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 

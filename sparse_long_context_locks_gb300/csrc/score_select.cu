@@ -419,6 +419,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // One cluster of C CTAs per (request, KV head).
 template <int C>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) select_kernel(const SelectParams p) {
+  // launched as a programmatic dependent of the scoring pass, and the split-K
+  // attention as one of this kernel
+  griddep_launch_dependents();
+  griddep_wait();
   // [slice keys][selected list]
   extern __shared__ __align__(16) uint32_t sel_dyn[];
   const int slice_cap = (p.max_pages + C - 1) / C;
@@ -459,8 +463,18 @@ cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t strea
   static DynSmemAttr smem_attr;
   const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C>), dyn, smem_attr);
   if (e != cudaSuccess) return e;
-  dim3 grid(C, units);
-  select_kernel<C><<<grid, kSelThreads, dyn, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, units, 1);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, select_kernel<C>, p);
+  if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 

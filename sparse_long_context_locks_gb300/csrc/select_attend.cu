@@ -37,7 +37,6 @@ constexpr int kFusedExtraWarps = 2;
 constexpr int kFusedMaxStages = kFusedStages + 1;
 constexpr int kFusedExtra = kFusedExtraWarps * kStageBytes;             // 16 KB
 
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Dynamic shared memory: [ring (keys and block ids of the slice during the
 // selection)] [selected blocks (rank 0)] [barriers]
