@@ -248,9 +248,69 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
   __syncthreads();
 
   // This CTA's contiguous range of work items (one stage = pps pages of one
-  // (request, head group) unit each), split evenly over the grid.
-  const int it_begin = (int)(((long long)blockIdx.x * p.n_items) / gridDim.x);
-  const int it_end = (int)(((long long)(blockIdx.x + 1) * p.n_items) / gridDim.x);
+  // (request, head group) unit; unit u owns items [u n_chunks, (u + 1)
+  // n_chunks)), split evenly over the grid.  With one unit the split is over
+  // all of them (at most one past its full pages).  With several, requests of
+  // different lengths leave different numbers of items empty, so warp 0
+  // counts each unit's items that hold full pages (from the sequence
+  // lengths), splits that count evenly, and maps the CTA's share back to item
+  // indices; the loops below skip the empty items in between.
+  int it_begin = (int)(((long long)blockIdx.x * p.n_items) / gridDim.x);
+  int it_end = (int)(((long long)(blockIdx.x + 1) * p.n_items) / gridDim.x);
+  const int n_units = p.batch * p.head_groups;
+  if (n_units > 1) {
+    __shared__ int s_range[2];
+    if (warp == 0) {
+      auto items_of = [&](int u) -> int {   // items of unit u holding full pages
+        if (u >= n_units) return 0;
+        const int nf = request_full_pages(p, u / p.head_groups);
+        if (nf < 0 && blockIdx.x == 0 && u % p.head_groups == 0) flag_status(p.status, LOCKS_FLAG_BAD_SEQLEN);
+        return (max(nf, 0) + kPps - 1) / kPps;
+      };
+      long long total = 0;
+      for (int base = 0; base < n_units; base += 32) {
+        int v = items_of(base + lane);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        total += v;
+      }
+      const long long x0 = (long long)blockIdx.x * total / gridDim.x;
+      const long long x1 = (long long)(blockIdx.x + 1) * total / gridDim.x;
+      // item index of compact position x: unit u with prefix <= x < prefix + count
+      int r0 = p.n_items, r1 = p.n_items;
+      long long prefix = 0;
+      for (int base = 0; base < n_units && (r0 == p.n_items || r1 == p.n_items); base += 32) {
+        const int v = items_of(base + lane);
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const long long lo = prefix + incl - v, hi = prefix + incl;   // this lane's unit: [lo, hi)
+        const uint32_t in0 = __ballot_sync(0xffffffffu, v > 0 && x0 >= lo && x0 < hi);
+        const uint32_t in1 = __ballot_sync(0xffffffffu, v > 0 && x1 >= lo && x1 < hi);
+        if (in0 && r0 == p.n_items) {
+          const int l = __ffs(in0) - 1;
+          const long long lo_l = __shfl_sync(0xffffffffu, lo, l);
+          r0 = (base + l) * p.n_chunks + (int)(x0 - lo_l);
+        }
+        if (in1 && r1 == p.n_items) {
+          const int l = __ffs(in1) - 1;
+          const long long lo_l = __shfl_sync(0xffffffffu, lo, l);
+          r1 = (base + l) * p.n_chunks + (int)(x1 - lo_l);
+        }
+        prefix += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        s_range[0] = r0;
+        s_range[1] = r1;
+      }
+    }
+    __syncthreads();
+    it_begin = s_range[0];
+    it_end = s_range[1];
+  }
   const int first_unit = it_begin / p.n_chunks;
 
   if (warp == kScoreConsumers) {
