@@ -131,18 +131,21 @@ struct ClusterSel {
 //   keys_s   ceil(max_pages / C) <= kFusedMaxKeysPerCta words: this CTA's keys;
 //   bt_slice optional block ids of this CTA's pages (nullptr: none);
 //   out_blk  budget words, used on rank 0: the selected pages' physical
-//            blocks (bt_slice given) or page indices, ascending by page.
+//            blocks (bt_slice given) or page indices, ascending by page;
+//   stage    room for this CTA's slice of scores (used when kStaged; else
+//            both passes over the scores read them from global memory).
 struct SelScratch {
   uint32_t* keys_s;
   const int* bt_slice;
   int* out_blk;
+  float4* stage;
 };
 
 // Selects the pages of unit (b, h) = blockIdx.y.  Every thread of every CTA
 // of the cluster must call it.  Writes `selected` and `n_selected`; ends with
 // a cluster barrier after which rank 0's out_blk[0, kk) may be read through
 // distributed shared memory.
-template <int C>
+template <int C, bool kStaged>
 static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScratch& sc) {
   __shared__ __align__(16) int hist0[1 << 11];
   __shared__ __align__(16) int hist1[1 << 10];
@@ -196,12 +199,21 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
 
   // ---- 1. this slice's (max, sum) of the scores per head, log2 units
   const float4* srow = reinterpret_cast<const float4*>(p.scores + (int64_t)unit * p.max_pages * kGroup) + j0;
+  // Staged: every thread copies the scores it will read (its own indices in
+  // both passes) with asynchronous copies, so the whole slice is in flight at
+  // once instead of a few loads per thread.
+  const float4* src = kStaged ? sc.stage : srow;
+  if constexpr (kStaged) {
+    for (int i = tid; i < len; i += blockDim.x) cp_async16(&sc.stage[i], &srow[i]);
+  }
   constexpr int kPre = 4;   // scores held in registers for both passes
   float4 pre[kPre];
+  if constexpr (!kStaged) {
 #pragma unroll
-  for (int r = 0; r < kPre; ++r) {
-    const int i = tid + r * kSelThreads;
-    pre[r] = i < len ? srow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < kPre; ++r) {
+      const int i = tid + r * kSelThreads;
+      pre[r] = i < len ? srow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   for (int i = tid; i < (1 << 10); i += blockDim.x) {
     hist1[i] = 0;
@@ -209,23 +221,50 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
   }
   for (int i = tid; i < (1 << 11); i += blockDim.x) hist0[i] = 0;
   if (tid == 0) s_hmax = -1;
+  if constexpr (kStaged) {
+    cp_async_wait_all();
+#pragma unroll
+    for (int r = 0; r < kPre; ++r) {
+      const int i = tid + r * kSelThreads;
+      pre[r] = i < len ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   {
     float m[kGroup] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     float s[kGroup] = {0.f, 0.f, 0.f, 0.f};
-    auto fold = [&](const float4& v) {
-      const float x[kGroup] = {v.x * kLog2e, v.y * kLog2e, v.z * kLog2e, v.w * kLog2e};
+    // fold kPre scores (an absent one is -inf) into (m, s): the batch's max
+    // per head first, then one rescale of s and kPre independent terms
+    auto fold_batch = [&](const float4 (&v)[kPre], int cnt) {
 #pragma unroll
       for (int g = 0; g < kGroup; ++g) {
-        const float mn = fmaxf(m[g], x[g]);
-        s[g] = s[g] * fast_exp2(m[g] - mn) + fast_exp2(x[g] - mn);
-        m[g] = mn;
+        float x[kPre];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+          const float c = g == 0 ? v[k].x : g == 1 ? v[k].y : g == 2 ? v[k].z : v[k].w;
+          x[k] = k < cnt ? c * kLog2e : -INFINITY;
+        }
+        float mn = m[g];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) mn = fmaxf(mn, x[k]);
+        if (mn != -INFINITY) {
+          float acc = s[g] * fast_exp2(m[g] - mn);
+#pragma unroll
+          for (int k = 0; k < kPre; ++k) acc += fast_exp2(x[k] - mn);
+          s[g] = acc;
+          m[g] = mn;
+        }
       }
     };
+    fold_batch(pre, min(kPre, max(0, (len - tid + kSelThreads - 1) / kSelThreads)));
+    for (int i0 = tid + kPre * kSelThreads; i0 < len; i0 += kPre * kSelThreads) {
+      float4 v[kPre];
 #pragma unroll
-    for (int r = 0; r < kPre; ++r)
-      if (tid + r * kSelThreads < len) fold(pre[r]);
-#pragma unroll 4
-    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) fold(srow[i]);
+      for (int k = 0; k < kPre; ++k) {
+        const int i = i0 + k * kSelThreads;
+        v[k] = i < len ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      fold_batch(v, min(kPre, (len - i0 + kSelThreads - 1) / kSelThreads));
+    }
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       float mx = m[g];
@@ -282,7 +321,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       if (i < len) make_key(pre[r], i);
     }
 #pragma unroll 4
-    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) make_key(srow[i], i);
+    for (int i = tid + kPre * kSelThreads; i < len; i += blockDim.x) make_key(src[i], i);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     if (__any_sync(0xffffffffu, any) && lane == 0) atomicMax(&s_hmax, (int)lvl_digit(kmax, 0));

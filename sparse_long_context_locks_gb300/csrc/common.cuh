@@ -53,11 +53,17 @@ constexpr int kFusedMaxKeysPerCta = 16384; // keys per selecting CTA (fused: key
 constexpr int kFusedMaxBudget = 2047;      // fused pass: <= 32 items per warp of 64
 constexpr int kSmemLimit = 200 * 1024;     // dynamic shared memory we allow a CTA (static <= 27 KB)
 
-// Dynamic shared memory of the selection kernel: slice keys and the selected
-// list (rank 0).
-__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget, int cluster = kSelCluster) {
+// Dynamic shared memory of the selection kernel: slice keys, the selected
+// list (rank 0) and, when staged, the slice's scores (16 bytes a page).
+__host__ __device__ inline size_t select_stage_offset(int max_pages, int budget, int cluster) {
   const int slice_cap = (max_pages + cluster - 1) / cluster;
-  return 4 * ((size_t)slice_cap + (size_t)budget + 4);
+  return (4 * ((size_t)slice_cap + (size_t)budget + 4) + 15) / 16 * 16;
+}
+__host__ __device__ inline size_t select_smem_bytes(int max_pages, int budget, int cluster = kSelCluster,
+                                                    bool stage = false) {
+  const int slice_cap = (max_pages + cluster - 1) / cluster;
+  return stage ? select_stage_offset(max_pages, budget, cluster) + 16 * (size_t)slice_cap
+               : 4 * ((size_t)slice_cap + (size_t)budget + 4);
 }
 
 // ---------------------------------------------------------------- status
@@ -133,6 +139,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ---------------------------------------------------------------- TMA
+// 16-byte asynchronous copy global -> shared, completed by cp_async_wait_all
+// in the issuing thread.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Untiled bulk copy global -> shared; completes `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
                                          uint64_t* bar) {

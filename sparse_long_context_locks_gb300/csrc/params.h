@@ -34,6 +34,7 @@ struct SelectParams {
   int32_t* n_selected;     // [batch][H_kv]
   uint32_t* status;
   int batch, max_pages, H_kv, budget;
+  int stage_scores;        // 1: each CTA copies its slice of scores to shared memory first
 };
 
 struct AttnParams {

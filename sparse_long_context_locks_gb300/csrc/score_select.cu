@@ -477,20 +477,24 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 
 
 // One cluster of C CTAs per (request, KV head).
-template <int C>
+// kStaged: each CTA first copies its slice of scores to shared memory.
+template <int C, bool kStaged>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) select_kernel(const SelectParams p) {
   // launched as a programmatic dependent of the scoring pass, and the split-K
   // attention as one of this kernel
   griddep_launch_dependents();
   griddep_wait();
-  // [slice keys][selected list]
+  // [slice keys][selected list][slice scores, when staged]
   extern __shared__ __align__(16) uint32_t sel_dyn[];
   const int slice_cap = (p.max_pages + C - 1) / C;
   SelScratch sc;
   sc.keys_s = sel_dyn;
   sc.bt_slice = nullptr;
   sc.out_blk = reinterpret_cast<int*>(sel_dyn + slice_cap);
-  cluster_select<C>(p, sc);
+  sc.stage = kStaged ? reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(sel_dyn) +
+                                                 select_stage_offset(p.max_pages, p.budget, C))
+                     : nullptr;
+  cluster_select<C, kStaged>(p, sc);
 }
 
 }  // namespace locks
@@ -517,11 +521,11 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
   }
 }
 
-template <int C>
+template <int C, bool kStaged>
 cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t stream) {
-  const size_t dyn = select_smem_bytes(p.max_pages, p.budget, C);
+  const size_t dyn = select_smem_bytes(p.max_pages, p.budget, C, kStaged);
   static DynSmemAttr smem_attr;
-  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C>), dyn, smem_attr);
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C, kStaged>), dyn, smem_attr);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, units, 1);
@@ -533,17 +537,18 @@ cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t el = cudaLaunchKernelEx(&cfg, select_kernel<C>, p);
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, select_kernel<C, kStaged>, p);
   if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 
 cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream) {
+  const bool staged = p.stage_scores != 0;
   switch (cluster) {
-    case 8: return launch_select_c<8>(p, units, stream);
-    case 4: return launch_select_c<4>(p, units, stream);
-    case 2: return launch_select_c<2>(p, units, stream);
-    case 1: return launch_select_c<1>(p, units, stream);
+    case 8: return staged ? launch_select_c<8, true>(p, units, stream) : launch_select_c<8, false>(p, units, stream);
+    case 4: return staged ? launch_select_c<4, true>(p, units, stream) : launch_select_c<4, false>(p, units, stream);
+    case 2: return staged ? launch_select_c<2, true>(p, units, stream) : launch_select_c<2, false>(p, units, stream);
+    case 1: return staged ? launch_select_c<1, true>(p, units, stream) : launch_select_c<1, false>(p, units, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -100,7 +100,8 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   sc.keys_s = reinterpret_cast<uint32_t*>(smem);
   sc.bt_slice = bt_slice;
   sc.out_blk = list;
-  const ClusterSel cs = cluster_select<kSelCluster>(p.sel, sc);
+  sc.stage = nullptr;
+  const ClusterSel cs = cluster_select<kSelCluster, false>(p.sel, sc);
   fence_proxy_async_smem();   // generic writes to the ring before the tensor copies reuse it
   __syncthreads();
 

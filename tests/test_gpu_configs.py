@@ -73,6 +73,21 @@ def test_ctx1m_all_heads():
     _free(run)
 
 
+def test_staged_selection_ragged_requests():
+    """Requests of 70K-300K tokens: 2,344-page slices per selecting CTA, so
+    the selection kernel copies each CTA's scores to shared memory first; the
+    shorter requests leave slices with ragged ends and under 1,024 pages."""
+    w = W.Workload("ragged_300k", batch=3, context=70000, context_hi=300000, num_kv_heads=8, group=4,
+                   budget_tokens=2048, carriers_per_head=8, seed=105)
+    run = Run(w)
+    assert run.status == 0
+    assert len(set(run.lens)) == 3 and min(run.lens) // 16 < 8 * 1024 < w.max_pages
+    for b in range(w.batch):
+        for h in range(8):
+            check_unit(run, b, h, check_scores_too=(h == b))
+    _free(run)
+
+
 @pytest.mark.parametrize("regime", ["batch64_256k_lowrank", "batch64_256k_fullrank"])
 def test_batch64_256k_sampled_requests(regime):
     run = Run(W.CONFIGS[regime])
