@@ -215,6 +215,36 @@ def test_score_worked_example_golden_exact_and_quantised():
     np.testing.assert_allclose(got_q, g["expected_s_hat"], atol=g["tolerance_quantised"])
 
 
+def _quantised_generic_pages():
+    rng = _rng(13)
+    K = np.stack([_lowrank_page(rng, 8, noise=0.05) for _ in range(5)] +
+                 [rng.normal(size=(B, D)) for _ in range(3)])
+    q = rng.normal(size=(4, D)) * 2.0
+    return K, q, O.dequantize(O.decode_records(O.build_records(K)))
+
+
+def _reconstruction_pin_holds(score_fn) -> bool:
+    """The factored score q.mu + (V^T q).c_i equals, by linearity, attention
+    to the 16 keys the summary reconstructs, k_i = mu + V c_i: those keys are
+    formed explicitly and their log-sum-exp taken by torch (fp64, CPU)."""
+    K, q, dq = _quantised_generic_pages()
+    got = score_fn(q, dq["mu"], dq["V"], dq["C"])
+    keys = dq["mu"][:, None, :] + np.einsum("pdr,pir->pid", dq["V"], dq["C"])   # [page, token, dim]
+    logits = torch.from_numpy(np.einsum("gd,pid->pgi", q, keys) / math.sqrt(D))
+    want = torch.logsumexp(logits, dim=-1).numpy()
+    return bool(np.allclose(got, want, rtol=0, atol=1e-10))
+
+
+def test_score_quantised_generic_pages_are_the_lse_of_their_reconstructed_keys():
+    """Generic pages at rank 8 (five low-rank with noise, three iid), through
+    quantisation and the byte record."""
+    assert _reconstruction_pin_holds(O.page_scores)
+    # the quantised summary really is a different page from the original:
+    # the check is not the unquantised identity in disguise
+    K, q, dq = _quantised_generic_pages()
+    assert np.max(np.abs(O.page_scores(q, dq["mu"], dq["V"], dq["C"]) - O.exact_page_lse(q, K))) > 1e-4
+
+
 def test_score_heads_are_independent_and_equivariant():
     rng = _rng(12)
     K = rng.normal(size=(4, B, D))
@@ -417,6 +447,20 @@ def test_planted_mistakes_are_caught():
 
     for bad in (score_no_centroid, score_no_sqrt_d, score_mean_not_lse):
         assert not _score_pin_holds(bad), bad.__name__
+
+    # slips a one-page golden cannot see: another page's coefficients, and
+    # basis directions paired with the wrong coefficient columns
+    def score_neighbour_coefficients(q, mu, V, C):
+        return O.page_scores(q, mu, V, np.roll(C, 1, axis=0))
+
+    def score_reversed_directions(q, mu, V, C):
+        return O.page_scores(q, mu, V, C[:, :, ::-1])
+
+    assert _reconstruction_pin_holds(O.page_scores)
+    for bad in (score_no_centroid, score_no_sqrt_d, score_mean_not_lse, score_neighbour_coefficients,
+                score_reversed_directions):
+        assert not _reconstruction_pin_holds(bad), bad.__name__
+    assert _score_pin_holds(score_neighbour_coefficients)   # invisible to the one-page golden
 
     def select_unnormalised(s_hat, k):
         return O.select_pages(s_hat - s_hat.max(), k) if s_hat.shape[1] == 1 else \
