@@ -8,9 +8,9 @@
  *      reconstruction and selection (the equation for s_j(q)), group-shared
  *      selection (GQA), implementation notes (full CUDA graph, summaries built
  *      off the decode critical path when a page is finalised);
- *   abstract -- "estimates each page's attention mass by log-sum-exp, and
- *      attends only the top pages; selection itself reads no candidate keys
- *      or values" (paraphrased).
+ *   abstract -- the summary alone gives each page an estimate of its
+ *      attention mass (a log-sum-exp); only the highest-ranked pages are
+ *      attended, and ranking them touches no cached key or value.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -190,7 +190,7 @@ locks_status locks_score_select(const locks_cfg *cfg, const void *q, const void 
                                 int32_t *n_selected, void *workspace, size_t workspace_bytes,
                                 locks_stream_t stream);
 
-/* Sparse paged decode attention, §2 / abstract "attends only the top pages":
+/* Sparse paged decode attention, §2 / abstract (only the selected pages are read):
  * for each (b, h) and each of the G query heads of the group,
  * out = softmax(sm_scale * q K^T) V over the tokens of the selected full
  * pages plus the t_b tokens of the open tail page (always attended).  All G

@@ -15,11 +15,12 @@ Citations use the title of the source page and its section:
   [LOCKS §3]      the same summary, §3 "Main contributions" (Thm. 1: error
                   controlled by the spectral tail energy; page-local basis is
                   residual-optimal among orthogonal rank-r reconstructions).
-  [LOCKS abstract] the arXiv abstract: "estimates each page's attention mass by
-                  log-sum-exp, and attends only the top pages; selection itself
-                  reads no candidate keys or values" (paraphrased).
+  [LOCKS abstract] the arXiv abstract: each page's attention mass is
+                  estimated from its summary by a log-sum-exp, only the
+                  highest-ranked pages are attended, and ranking them reads no
+                  cached key or value.
 
-Readings of points the pages leave open (each listed in the design doc):
+Readings of points the pages leave open:
   * eigendecomposition of the 16x16 Gram matrix of the centred keys (same
     non-zero spectrum as the d x d covariance); eigenvalues <= 1e-6 * lambda_1
     give a zero basis column;
@@ -38,8 +39,10 @@ Readings of points the pages leave open (each listed in the design doc):
 Parity pins (tests/test_oracle_pins.py): every public function below is pinned
 against closed forms, hand-derived fixtures under tests/golden/, brute force or
 an independent library routine.  The quantised rank-8 score of a generic page
-has no printed value on the pages: its pin is the exact-quantisation worked
-example (tests/golden/score_two_level_page.txt) plus the closed form of the
+has no printed value on the pages: it is pinned to the log-sum-exp of the keys
+its summary reconstructs (linearity of the score equation, evaluated by
+torch), to the exact-quantisation worked example
+(tests/golden/score_two_level_page.json) and to the closed form of the
 unquantised full-rank path.
 """
 

@@ -5,7 +5,8 @@
 // Decoding", technical summary §2 ("Reconstruction and selection",
 // "Group-shared selection (GQA)", and the implementation note that the whole
 // decode step -- scoring, selection and sparse attention -- runs back to back
-// without host round trips) and the abstract ("attends only the top pages").
+// without host round trips) and the abstract (attention reads the selected
+// pages only).
 //
 // The cluster's 8 CTAs first run cluster_select (rank 0 ends up holding the
 // physical blocks of the selected pages; the block-table entries were fetched
