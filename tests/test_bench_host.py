@@ -44,3 +44,28 @@ def test_summary_median_max_and_active_reasons():
 def test_summary_without_samples_says_so():
     s = bench.ClockSampler.summary([])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == ["no samples"]
+
+
+def test_cpu_baseline_unit_runs_the_whole_oracle_path(tmp_path):
+    """The timed CPU baseline's unit of work is the oracle's score, select and
+    attend of one (request, KV head), on the host copies bench.py writes."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from sparse_long_context_locks_gb300 import workload as W
+
+    w = W.Workload("tiny", batch=2, context=700, context_hi=900, num_kv_heads=2, group=4,
+                   budget_tokens=16 * 6, carriers_per_head=2, seed=5)
+    d = W.generate(w, device="cpu")
+    kc = d["k_cache"].float().numpy()
+    summ = torch.from_numpy(O.build_records(kc.astype(np.float64)))
+    bench.oracle_host_copy(d, summ, str(tmp_path))
+    want = O.decode_step(d["q"].float().numpy(), kc, d["v_cache"].float().numpy(),
+                         d["block_table"].numpy().astype(np.int64), d["seq_lens"].numpy(),
+                         summ.numpy(), w.num_kv_heads, w.group, w.budget_pages)
+    for b in range(w.batch):
+        for h in range(w.num_kv_heads):
+            secs, abs_sum = bench._oracle_unit((str(tmp_path), b, h, w.group, w.budget_pages))
+            assert secs > 0
+            assert abs_sum == float(np.abs(want[(b, h)]["out"]).sum())
