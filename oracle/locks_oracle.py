@@ -36,11 +36,13 @@ Readings of points the pages leave open:
   * the token budget counts full pages only; the partially filled tail page
     (no summary yet) is always attended.
 
-Parity pins (tests/test_oracle_pins.py): every public function below is pinned
-against closed forms, hand-derived fixtures under tests/golden/, brute force or
-an independent library routine.  The quantised rank-8 score of a generic page
-has no printed value on the pages: it is pinned to the log-sum-exp of the keys
-its summary reconstructs (linearity of the score equation, evaluated by
+Parity pins (tests/test_oracle_pins.py, tests/test_oracle_step_pins.py): every
+public function below is pinned against closed forms, hand-derived fixtures
+under tests/golden/, brute force, an independent library routine, or (for the
+whole-step functions unit_scores_from_records and decode_step) a paged cache
+whose scores, selection and attention are gathered by hand.  The quantised
+rank-8 score of a generic page has no printed value on the pages: it is
+pinned to the log-sum-exp of the keys its summary reconstructs (linearity of the score equation, evaluated by
 torch), to the exact-quantisation worked example
 (tests/golden/score_two_level_page.json) and to the closed form of the
 unquantised full-rank path.
