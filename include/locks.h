@@ -27,6 +27,8 @@
  *    ran out) never fault: the kernel skips the offending access and ORs a
  *    LOCKS_FLAG_* bit into the status word at the start of `workspace`;
  *    locks_read_status() returns it (that call synchronises `stream`).
+ *    Every wait on an mbarrier is bounded (about one second of %globaltimer);
+ *    when one runs out the kernel flags LOCKS_FLAG_TIMEOUT and returns.
  *  - Fixed shape: head_dim d = 128, page_size B = 16, rank r = 8, quantised
  *    summaries; group_size G = 4.  Other values return LOCKS_ERR_UNSUPPORTED.
  *
@@ -95,7 +97,8 @@ typedef enum {
   LOCKS_ERR_UNSUPPORTED = 2,  /* a shape this build does not implement */
   LOCKS_ERR_WORKSPACE = 3,    /* workspace smaller than locks_workspace_bytes */
   LOCKS_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
-  LOCKS_ERR_TIMEOUT = 5       /* reserved: returned by locks_read_status callers */
+  LOCKS_ERR_TIMEOUT = 5       /* locks_read_status / locks_noalloc_read_status: the flags
+                                 read include LOCKS_FLAG_TIMEOUT (they are still returned) */
 } locks_status;
 
 typedef struct {
@@ -128,8 +131,24 @@ locks_status locks_workspace_bytes(const locks_cfg *cfg, int32_t batch, int32_t 
  * every call).  Enqueues one memset on `stream`. */
 locks_status locks_workspace_init(void *workspace, size_t workspace_bytes, locks_stream_t stream);
 
-/* Synchronise `stream`, copy the status word to *flags and clear it. */
+/* Synchronise `stream`, copy the status word to *flags and clear it.
+ * Returns LOCKS_ERR_TIMEOUT (with *flags written) when a bounded wait ran
+ * out since the last read, LOCKS_OK otherwise. */
 locks_status locks_read_status(void *workspace, uint32_t *flags, locks_stream_t stream);
+
+/* Diagnostic of the bounded waits (the paper has no counterpart): one CTA
+ * runs the library's bounded mbarrier wait on a barrier that never completes
+ * (it waits for two arrivals and gets one), with a limit of limit_us
+ * microseconds (1 .. 100000), after issuing one 256-byte bulk copy from `src`
+ * (device, 16-byte aligned) into shared memory on a second barrier.  The wait
+ * gives up after the limit and ORs LOCKS_FLAG_TIMEOUT into the status word at
+ * the start of `workspace`; the kernel then waits for its copy and returns, so
+ * the context stays usable.  result (device uint32[4], 16-byte aligned):
+ * [0] = 1 if the wait ran out, [1] = 1 if the copy landed, [2] = the sum of
+ * the 64 copied 32-bit words, [3] = low bits of the %globaltimer when the wait
+ * gave up. */
+locks_status locks_check_bounded_wait(const void *src, uint32_t *result, uint32_t limit_us, void *workspace,
+                                      size_t workspace_bytes, locks_stream_t stream);
 
 /* Page summary builder, §2 "page-local spectral decomposition" and
  * "quantisation": for each of the n_build physical blocks in block_ids
@@ -248,21 +267,30 @@ locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void 
  * has no counterpart: this exists for callers that cannot allocate device
  * memory (an engine that gave all of HBM to its KV-cache pool, a
  * latency-critical path where cudaMalloc would synchronise the device, a host
- * integration with no allocator).  Same computation, arguments and layouts as
- * locks_sparse_decode; the scratch (split partials, merge tickets, status
- * word) is one fixed 8 MiB device array inside the library, resident on every
- * GPU that loads it until exit.  Allocates nothing.  The first call on a
- * device looks up that array's address (make it before any stream capture);
- * each call clears the tickets and status with one cudaMemsetAsync on
- * `stream`.  Calls share the array: calls that overlap on the GPU race.
- * Returns LOCKS_ERR_WORKSPACE when batch * H_kv * splits partial states do
- * not fit in 8 MiB (e.g. beyond ~4000 request-head-split slots). */
+ * integration with no allocator).  Same computation, arguments, layouts,
+ * validation and split-K plan as locks_sparse_decode; the scratch (split
+ * partials, merge tickets, status word) is one fixed 8 MiB device array
+ * inside the library, resident on every GPU that loads it until exit.
+ * Allocates nothing.  The first call in a CUDA context looks up that array's
+ * address there (make it before any stream capture); each call clears the
+ * merge tickets with one cudaMemsetAsync on `stream`.  Device-side flags
+ * (LOCKS_FLAG_*) accumulate in the array's status word until
+ * locks_noalloc_read_status reads and clears them.  Calls share the array:
+ * calls that overlap on the GPU race.  Returns LOCKS_ERR_WORKSPACE, before
+ * any CUDA call, when batch * num_kv_heads exceeds 4025 (request, KV head)
+ * units, the most whose partial states fit in 8 MiB. */
 locks_status locks_sparse_decode_noalloc(const locks_cfg *cfg, const void *q, const void *k_cache,
                                          const void *v_cache, int64_t num_blocks,
                                          const int32_t *block_table, const int32_t *seq_lens,
                                          const int32_t *selected, const int32_t *n_selected,
                                          int32_t batch, int32_t max_pages, int32_t budget_pages,
                                          float sm_scale, float *out, locks_stream_t stream);
+
+/* Status word of locks_sparse_decode_noalloc, without a workspace: synchronise
+ * `stream`, copy the flags accumulated by the calls since the last read to
+ * *flags and clear them; LOCKS_ERR_TIMEOUT as for locks_read_status.  The
+ * paper has no counterpart (see above). */
+locks_status locks_noalloc_read_status(uint32_t *flags, locks_stream_t stream);
 
 /* Static description of a status code. */
 const char *locks_status_str(locks_status status);

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "liblocks.so")
-SOURCES = ["api.cu", "build_summaries.cu", "score_select.cu", "decode_attention.cu", "noalloc.cu", "select_attend.cu"]
+SOURCES = ["api.cu", "build_summaries.cu", "score_select.cu", "decode_attention.cu", "noalloc.cu",
+           "select_attend.cu", "wait_check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

@@ -17,7 +17,35 @@
 #include "../../include/locks.h"
 #include "common.cuh"
 
+#include "host_plan.h"
 #include "params.h"
+
+namespace locks {
+
+bool cfg_supported(const locks_cfg* c) {
+  if (c == nullptr) return false;
+  if (c->head_dim != kHeadDim || c->page_size != kPage || c->rank != kRank) return false;
+  if (c->quant != 1 || c->group_size != kGroup) return false;
+  const int H = c->num_kv_heads;
+  if (H < 1) return false;
+  const int h_cta = H < 8 ? H : 8;
+  return (8 % h_cta == 0) && (H % h_cta == 0);
+}
+
+// Sparse units all hold about budget + 1 items, so the split is sized for
+// one wave: every CTA resident at once, each with the longest slice (and at
+// least one item per warp).  Measured at batch 16: 0.59 of peak against 0.34
+// with eight waves of short CTAs.
+void sparse_split(int64_t units, int budget_pages, int* splits, int* items_per_split) {
+  const int64_t items = (int64_t)budget_pages + 1;
+  const int64_t by_items = (items + 3) / 4;
+  const int64_t want = kTargetCtas / (units > 0 ? units : 1);
+  const int64_t sp = by_items < want ? by_items : want;
+  *splits = (int)(sp > 1 ? sp : 1);
+  *items_per_split = (int)((items + *splits - 1) / *splits);
+}
+
+}  // namespace locks
 
 namespace {
 
@@ -35,16 +63,6 @@ struct Plan {
   // workspace regions
   size_t off_scores, off_attn, off_tickets, total;
 };
-
-bool cfg_supported(const locks_cfg* c) {
-  if (c == nullptr) return false;
-  if (c->head_dim != kHeadDim || c->page_size != kPage || c->rank != kRank) return false;
-  if (c->quant != 1 || c->group_size != kGroup) return false;
-  const int H = c->num_kv_heads;
-  if (H < 1) return false;
-  const int h_cta = H < 8 ? H : 8;
-  return (8 % h_cta == 0) && (H % h_cta == 0);
-}
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
@@ -71,13 +89,7 @@ Plan make_plan(const locks_cfg* c, int batch, int max_pages, int budget) {
   pl.n_items = (int)items;
   pl.score_grid = (int)(items < kTargetCtas ? items : kTargetCtas);
   const int units = batch * H;
-  // Sparse units all hold about budget + 1 items, so the split is sized for
-  // one wave: every CTA resident at once, each with the longest slice (and
-  // at least one item per warp).  Measured at batch 16: 0.59 of peak against
-  // 0.34 with eight waves of short CTAs.  The dense units vary with the
-  // context, and keep eight waves for balance.
-  pl.sparse_splits = max(1, min(ceil_div(budget + 1, 4), kTargetCtas / max(1, units)));
-  pl.sparse_ips = ceil_div(budget + 1, pl.sparse_splits);
+  sparse_split(units, budget, &pl.sparse_splits, &pl.sparse_ips);
   // Dense units vary with the context, so larger batches keep about eight
   // waves for balance (batch 16: 0.98 of peak, against 0.94 with one wave);
   // a few units would leave eight waves of very short CTAs, so they take one
@@ -157,7 +169,11 @@ bool select_stage(int units, int cluster, int max_pages, int budget) {
 
 uint32_t* status_word(void* ws) { return ws ? reinterpret_cast<uint32_t*>(ws) : nullptr; }
 
+}  // namespace
+
 // ---------------------------------------------------------------- tensor maps
+namespace locks {
+namespace {
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -177,8 +193,8 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D view of a [num_blocks][H][16][128] bf16 cache: rows = page-head tokens,
-// 128 columns; boxes of 16 rows x 64 columns with 128-byte swizzle.
+}  // namespace
+
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int H) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
@@ -191,6 +207,12 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, in
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+}  // namespace locks
+
+namespace {
+
+using namespace locks;
 
 locks_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
 
@@ -277,7 +299,7 @@ locks_status locks_read_status(void* workspace, uint32_t* flags, locks_stream_t 
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return LOCKS_ERR_CUDA;
   *flags = v;
-  return LOCKS_OK;
+  return (v & LOCKS_FLAG_TIMEOUT) ? LOCKS_ERR_TIMEOUT : LOCKS_OK;
 }
 
 locks_status locks_build_summaries(const locks_cfg* cfg, const void* k_cache, int64_t num_blocks,

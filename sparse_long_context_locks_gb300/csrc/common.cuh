@@ -125,13 +125,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: true once the phase with this parity completed, false (and
-// LOCKS_FLAG_TIMEOUT recorded) after about one second.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// LOCKS_FLAG_TIMEOUT recorded) after limit_ns of %globaltimer (one second by
+// default; every wait in the decode kernels uses the default).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > 1000000000ull) {
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
       flag_status(status, LOCKS_FLAG_TIMEOUT);
       return false;
     }

@@ -1,32 +1,36 @@
-// noalloc.cu -- locks_sparse_decode_noalloc: sparse decode attention that
-// needs no caller-provided workspace.
+// noalloc.cu -- locks_sparse_decode_noalloc and locks_noalloc_read_status:
+// sparse decode attention that needs no caller-provided workspace.
 //
 // Some callers cannot allocate device memory at all: a serving engine that has
 // handed all of HBM to its KV-cache pool, code on a latency-critical path where
 // a cudaMalloc would synchronise the device, or a host integration with no
 // allocator of its own.  This entry point runs the same split-K attention
-// kernel as locks_sparse_decode, but its scratch (per-split partial softmax
-// states, merge tickets and the status word) lives in one file-scope device
-// array of fixed size that every GPU loading the library holds until the
-// process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
+// kernel as locks_sparse_decode, with the same validation and the same split
+// of each unit's items (host_plan.h), but its scratch (per-split partial
+// softmax states, merge tickets and the status word) lives in one file-scope
+// device array of fixed size that every GPU loading the library holds until
+// the process exits.  It calls no cudaMalloc, cudaFree or allocating routine.
 //
-// Set-up: the first call on a device looks up the array's device address with
-// cudaGetSymbolAddress (the host-side symbol is only a stand-in, never a device
-// pointer) and caches it per device; make that first call before any stream
-// capture.  Every call clears the status word and the tickets with one
-// cudaMemsetAsync on `stream`.  All calls share the one array and it keeps the
-// last call's contents, so calls that overlap on the GPU (two streams, two
-// host threads) race on it: serialise them.
+// Set-up: in host code the array's name is only a stand-in, never a device
+// address.  The first call in a CUDA context looks up the array's device
+// address there with cudaGetSymbolAddress and keeps it, keyed by the
+// context's unique id (a context created after cudaDeviceReset, or another
+// context made current, gets its own look-up); make that first call before any
+// stream capture.  Every call clears the merge tickets with one cudaMemsetAsync
+// on `stream`; the status word keeps accumulating flags until
+// locks_noalloc_read_status reads and clears it.  All calls share the one
+// array and it keeps the last call's contents, so calls that overlap on the
+// GPU (two streams, two host threads) race on it: serialise them.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/locks.h"
 #include "common.cuh"
+#include "host_plan.h"
 #include "params.h"
 
 namespace {
@@ -35,56 +39,85 @@ using namespace locks;
 
 constexpr size_t kScratchBytes = size_t(8) << 20;   // 8 MiB per device
 constexpr size_t kHeaderBytes = 256;                 // status word
+constexpr size_t kPartBytes = (size_t)kGroup * (2 + kHeadDim) * sizeof(float);   // one split's state
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// ---- the array's device address, per CUDA context
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device (looked up once).
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+struct DriverFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns() {
+  static DriverFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return fns;
+}
+
+constexpr int kCacheSlots = 64;
+struct AddrSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+std::mutex g_mu;
+AddrSlot g_slots[kCacheSlots] = {};
+int g_next_slot = 0;
+
+// Unique id of the current CUDA context, 0 if none is current or the driver
+// entry points are missing.
+unsigned long long current_ctx_id() {
+  const DriverFns& fns = driver_fns();
+  unsigned long long id = 0;
+  CUcontext ctx = nullptr;
+  if (fns.get_current == nullptr || fns.get_id == nullptr) return 0;
+  if (fns.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current context.
+cudaError_t scratch_address(void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  unsigned long long id = current_ctx_id();
+  if (id != 0) {
+    for (const AddrSlot& s : g_slots)
+      if (s.ctx_id == id) {
+        *out = s.ptr;
+        return cudaSuccess;
+      }
   }
-  *out = g_scratch_ptr[dev];
+  // first use in this context (the look-up also makes the runtime's primary
+  // context current when none was)
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_ctx_id();
+  if (id != 0) {
+    g_slots[g_next_slot] = AddrSlot{id, p};
+    g_next_slot = (g_next_slot + 1) % kCacheSlots;
+  }
+  *out = p;
   return cudaSuccess;
 }
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                              CUtensorMapFloatOOBfill);
-
-bool encode_map(CUtensorMap* map, const void* base, int64_t num_blocks, int H) {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-  });
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(num_blocks * H * kPage)};
-  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  const cuuint32_t box[2] = {64, kPage};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool a16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t tickets_bytes(int64_t units) { return ((size_t)units * sizeof(uint32_t) + 255) / 256 * 256; }
 
 }  // namespace
 
@@ -94,9 +127,7 @@ extern "C" locks_status locks_sparse_decode_noalloc(
     const int32_t* n_selected, int32_t batch, int32_t max_pages, int32_t budget_pages, float sm_scale,
     float* out, locks_stream_t stream) {
   if (cfg == nullptr) return LOCKS_ERR_INVALID_ARG;
-  if (cfg->head_dim != kHeadDim || cfg->page_size != kPage || cfg->rank != kRank || cfg->quant != 1 ||
-      cfg->group_size != kGroup || cfg->num_kv_heads < 1)
-    return LOCKS_ERR_UNSUPPORTED;
+  if (!cfg_supported(cfg)) return LOCKS_ERR_UNSUPPORTED;
   const int H = cfg->num_kv_heads;
   if (batch < 0 || max_pages < 1 || budget_pages < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f)) return LOCKS_ERR_INVALID_ARG;
@@ -106,26 +137,23 @@ extern "C" locks_status locks_sparse_decode_noalloc(
     return LOCKS_ERR_INVALID_ARG;
   if (num_blocks * H * kPage >= (int64_t)1 << 31) return LOCKS_ERR_UNSUPPORTED;
 
-  // same split rule as the workspace entry point: one wave of resident CTAs,
-  // at least one item per warp
+  // the same split as the workspace entry point; the size check comes before
+  // any CUDA call
   const int64_t units = (int64_t)batch * H;
-  const int64_t items = (int64_t)budget_pages + 1;
-  const int64_t by_items = (items + 3) / 4;
-  const int64_t want = units > 0 ? kTargetCtas / units : 1;
-  const int splits = (int)std::max<int64_t>(1, std::min(by_items, want));
-  const int ips = (int)((items + splits - 1) / splits);
-  const size_t tickets_bytes = ((size_t)units * sizeof(uint32_t) + 255) / 256 * 256;
-  const size_t need = kHeaderBytes + tickets_bytes + (size_t)units * splits * kGroup * (2 + kHeadDim) * sizeof(float);
+  int splits = 1, ips = 1;
+  sparse_split(units, budget_pages, &splits, &ips);
+  const size_t tb = tickets_bytes(units);
+  const size_t need = kHeaderBytes + tb + (size_t)units * (size_t)splits * kPartBytes;
   if (need > kScratchBytes) return LOCKS_ERR_WORKSPACE;   // batch too large for the fixed scratch
 
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return LOCKS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* scratch = static_cast<uint8_t*>(base);
-  if (cudaMemsetAsync(scratch, 0, kHeaderBytes + tickets_bytes, s) != cudaSuccess) return LOCKS_ERR_CUDA;
+  if (cudaMemsetAsync(scratch + kHeaderBytes, 0, tb, s) != cudaSuccess) return LOCKS_ERR_CUDA;
 
   CUtensorMap tmk, tmv;
-  if (!encode_map(&tmk, k_cache, num_blocks, H) || !encode_map(&tmv, v_cache, num_blocks, H))
+  if (!encode_cache_map(&tmk, k_cache, num_blocks, H) || !encode_cache_map(&tmv, v_cache, num_blocks, H))
     return LOCKS_ERR_CUDA;
   AttnParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -136,7 +164,7 @@ extern "C" locks_status locks_sparse_decode_noalloc(
   p.out = out;
   p.status = reinterpret_cast<uint32_t*>(scratch);
   p.tickets = reinterpret_cast<uint32_t*>(scratch + kHeaderBytes);
-  p.part = reinterpret_cast<float*>(scratch + kHeaderBytes + tickets_bytes);
+  p.part = reinterpret_cast<float*>(scratch + kHeaderBytes + tb);
   p.num_blocks = num_blocks;
   p.batch = batch;
   p.max_pages = max_pages;
@@ -147,4 +175,19 @@ extern "C" locks_status locks_sparse_decode_noalloc(
   p.items_per_split = ips;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   return launch_attn(tmk, tmv, p, s) == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA;
+}
+
+extern "C" locks_status locks_noalloc_read_status(uint32_t* flags, locks_stream_t stream) {
+  if (flags == nullptr) return LOCKS_ERR_INVALID_ARG;
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return LOCKS_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, base, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return LOCKS_ERR_CUDA;
+  *flags = v;
+  return (v & LOCKS_FLAG_TIMEOUT) ? LOCKS_ERR_TIMEOUT : LOCKS_OK;
 }

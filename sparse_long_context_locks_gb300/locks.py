@@ -67,6 +67,8 @@ _SIGS = {
     "locks_status_str": (ctypes.c_char_p, [_I32]),
     "locks_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32,
                                            _I32, _F, _P, _P]),
+    "locks_noalloc_read_status": (_I32, [ctypes.POINTER(ctypes.c_uint32), _P]),
+    "locks_check_bounded_wait": (_I32, [_P, _P, ctypes.c_uint32, _P, _SZ, _P]),
 }
 
 
@@ -130,10 +132,20 @@ def locks_workspace_init(workspace, stream=None) -> None:
                                        _stream(stream)), "locks_workspace_init")
 
 
+LOCKS_ERR_TIMEOUT = 5
+
+
+def _check_status_read(status: int, where: str) -> None:
+    # LOCKS_ERR_TIMEOUT only says that the flags read include FLAG_TIMEOUT
+    if status not in (LOCKS_OK, LOCKS_ERR_TIMEOUT):
+        raise LocksError(status, where)
+
+
 def locks_read_status(workspace, stream=None) -> int:
+    """Flags of the status word (read and cleared; synchronises the stream)."""
     v = ctypes.c_uint32(0)
-    _check(load().locks_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream)),
-           "locks_read_status")
+    _check_status_read(load().locks_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream)),
+                       "locks_read_status")
     return int(v.value)
 
 
@@ -346,6 +358,26 @@ def locks_sparse_decode_noalloc(num_kv_heads, q, k_cache, v_cache, block_table, 
         _ptr(block_table), _ptr(seq_lens), _ptr(selected), _ptr(n_selected),
         block_table.shape[0], block_table.shape[1], budget_pages, scale, _ptr(out),
         _stream(stream)), "locks_sparse_decode_noalloc")
+
+
+def locks_noalloc_read_status(stream=None) -> int:
+    """Flags accumulated by locks_sparse_decode_noalloc since the last read
+    (the read clears them); synchronises the stream."""
+    v = ctypes.c_uint32(0)
+    _check_status_read(load().locks_noalloc_read_status(ctypes.byref(v), _stream(stream)),
+                       "locks_noalloc_read_status")
+    return int(v.value)
+
+
+def locks_check_bounded_wait(src, result, limit_us, workspace, stream=None) -> None:
+    """Diagnostic: make one bounded wait run out after limit_us (see locks.h).
+    src: 256 bytes on the device; result: device int32/uint32 [4]."""
+    _req(src, "src", "uint8", (256,))
+    _req(result, "result", "int32", (4,))
+    _req(workspace, "workspace", "uint8")
+    _check(load().locks_check_bounded_wait(_ptr(src), _ptr(result), int(limit_us), _ptr(workspace),
+                                           _nbytes(workspace), _stream(stream)),
+           "locks_check_bounded_wait")
 
 
 def locks_status_str(status: int) -> str:

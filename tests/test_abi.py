@@ -82,6 +82,36 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.locks_read_status(None, ctypes.byref(v), None) == INVALID
 
 
+def test_noalloc_validates_like_the_workspace_entry_point_before_any_cuda_call(lib):
+    """The allocation-free entry point shares the workspace path's
+    configuration check and split plan, and rejects a batch whose partial
+    states exceed its fixed 8 MiB scratch before making any CUDA call (so this
+    runs without a GPU)."""
+    fake = ctypes.c_void_p(0x10000)
+    scale = ctypes.c_float(0.088)
+
+    def call(cfg, batch, budget=128):
+        return lib.locks_sparse_decode_noalloc(ctypes.byref(cfg), fake, fake, fake, 10, fake, fake, fake,
+                                               fake, batch, 8, budget, scale, fake, None)
+
+    # KV-head counts the scorer's head grouping cannot tile are rejected by
+    # both entry points
+    for H in (3, 12):
+        bad = L.locks_cfg(128, 16, 8, H, 4, 1)
+        assert call(bad, 1) == UNSUPPORTED
+        assert lib.locks_sparse_decode(ctypes.byref(bad), fake, fake, fake, 10, fake, fake, fake, fake, 1,
+                                       8, 2, scale, fake, fake, 1 << 20, None) == UNSUPPORTED
+    # 4025 (request, KV head) units fit, 4026 do not: the limit in locks.h
+    assert call(L.make_cfg(1), 4026) == WORKSPACE
+    assert call(L.make_cfg(2), 2013 + 1) == WORKSPACE     # 4028 units
+    assert call(L.make_cfg(8), 504) == WORKSPACE          # 4032 units
+    assert call(L.make_cfg(8), 10_000, budget=0) == WORKSPACE
+    # argument errors come first, as on the workspace path
+    assert lib.locks_sparse_decode_noalloc(ctypes.byref(L.make_cfg(8)), None, fake, fake, 10, fake, fake,
+                                           fake, fake, 600, 8, 128, scale, fake, None) == INVALID
+    assert lib.locks_noalloc_read_status(None, None) == INVALID
+
+
 def test_binding_raises_on_missing_library(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "LIB", str(tmp_path / "nope.so"))
     monkeypatch.setattr(L, "_lib", None)
