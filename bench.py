@@ -5,20 +5,28 @@ locks_decode_step = page scoring (locks_score) followed by group-shared top-k
 selection and sparse paged attention over the selected pages and the open tail
 page -- one fused cluster kernel when every (request, KV head) cluster fits on
 the GPU at once, else the selection kernel and split-K attention -- captured
-once into a CUDA graph and replayed.  The fused and the separate kernels are
-also timed on their own (rows "select_attend_fused_us", "select_us",
-"sparse_attention_us").  The
-summary builder (run when pages are finalised, off the decode critical path)
-and the dense comparator are timed in the same run and reported under "rows".
+once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload llama8b_128k]
+                  [--workload llama8b_128k] [--extra-workloads ctx1m,batch16_32k]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
 events on the launching stream; between timed steps L2 is flushed by reading a
 256 MB buffer (the step's inputs are smaller than L2), outside the events.
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling),
 the per-rank times are max-reduced and rank 0 prints one JSON line.
+
+Besides the contract's keys the line carries:
+  roofline          the dominant kernel of the step (the longest one timed
+                    alone): algorithmic bytes per launch / its event time,
+                    against the measured copy bandwidth;
+  roofline_kernels  the same for every kernel the step launches;
+  roofline_step     the whole step's algorithmic bytes / the step time;
+  rows              per-kernel event times, the dense comparator, the summary
+                    builder and the page-crossing step;
+  workloads         the step and per-kernel rows of the other workloads
+                    (default: one request at 1M tokens and batch 16 x 24-32K),
+                    measured in the same run.
 """
 
 from __future__ import annotations
@@ -37,19 +45,39 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-step µs/layer and tokens/s at 128K–1M ctx; achieved HBM GB/s vs peak"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_llama8b_128k.json")
-# every source the scoring kernel is compiled from: the ncu traffic figure is
-# used only while their combined hash matches the one it was captured with
-SCORE_SOURCES = [os.path.join(ROOT, "sparse_long_context_locks_gb300", "csrc", f)
-                 for f in ("score_select.cu", "common.cuh", "params.h", "cluster_select.cuh")]
+# DRAM bytes per launch of each kernel, from ncu captures (dram__bytes_read.sum
+# + dram__bytes_write.sum), keyed "<kernel>@<workload>".  An entry is used only
+# while the combined hash of the sources its kernel is compiled from matches
+# the hash recorded with it; otherwise "traffic" is null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+_CSRC = os.path.join(ROOT, "sparse_long_context_locks_gb300", "csrc")
+_COMMON = ("common.cuh", "params.h")
+KERNEL_SOURCES = {
+    "score_kernel": ("score_select.cu", "cluster_select.cuh") + _COMMON,
+    "select_kernel": ("score_select.cu", "cluster_select.cuh") + _COMMON,
+    "select_attend_kernel": ("select_attend.cu", "cluster_select.cuh", "attn_tile.cuh") + _COMMON,
+    "attn_kernel": ("decode_attention.cu", "attn_tile.cuh") + _COMMON,
+    "build_kernel": ("build_summaries.cu",) + _COMMON,
+}
 
 
-def score_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for path in SCORE_SOURCES:
-        with open(path, "rb") as f:
-            h.update(f.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entry = json.load(f)[f"{kernel}@{workload}"]
+    except Exception:
+        return None
+    if entry.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return entry.get("dram_bytes_per_launch")
 
 
 def parse():
@@ -61,6 +89,9 @@ def parse():
     ap.add_argument("--workload", default="llama8b_128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-workloads", default="ctx1m,batch16_32k",
+                    help="other named workloads whose step and per-kernel rows are measured in the "
+                         "same run (comma-separated; empty for none)")
     ap.add_argument("--profile-run", action="store_true",
                     help="warm-up and timed steps only (no per-kernel rows, e2e or CPU baseline): "
                          "the command the ncu captures run")
@@ -79,10 +110,13 @@ def peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms by a reader thread (read-only queries)."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampled every 100 ms by a reader thread (read-only queries).
+    A sample counts as under load when the GPU's utilisation over its sampling
+    period is at least LOAD_UTIL percent."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    LOAD_UTIL = 50.0
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -93,12 +127,13 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
+            if len(parts) < 11:
                 continue
             try:
                 self.rows.append({"sm": float(parts[2]), "max": float(parts[3]), "power": float(parts[4]),
-                                  "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
-                                  "sw_power": parts[9]})
+                                  "util": float(parts[5].rstrip("%").strip()),
+                                  "hw": parts[7], "hw_thermal": parts[8], "sw_thermal": parts[9],
+                                  "sw_power": parts[10]})
             except ValueError:
                 continue
 
@@ -133,8 +168,11 @@ class ClockSampler:
     @staticmethod
     def summary(rows):
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        load = [r for r in rows if r["power"] > 0] or rows
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "samples_under_load": 0}
+        load = [r for r in rows if r.get("util", 0.0) >= ClockSampler.LOAD_UTIL]
+        under = len(load)
+        load = load or rows
         sm = sorted(r["sm"] for r in load)
         reasons = set()
         for r in load:
@@ -143,7 +181,7 @@ class ClockSampler:
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r["max"] for r in load),
-                "reasons": sorted(reasons), "samples": len(load)}
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": under}
 
 
 # ------------------------------------------------------------------ oracle baseline
@@ -211,6 +249,98 @@ def make_pool():
     return ctx.Pool(cores), cores
 
 
+# ------------------------------------------------------------------ one workload's graphs
+class WorkloadCase:
+    """A workload's device buffers and its captured graphs: the whole decode
+    step (locks_decode_step) and each kernel of it on its own, plus the dense
+    comparator."""
+
+    def __init__(self, L, w, data, summ, bufs, capture):
+        import torch
+        self.w, self.data, self.bufs = w, data, bufs
+        H = w.num_kv_heads
+        self.H = H
+
+        def step_calls(s):
+            L.locks_decode_step(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
+                                data["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                                bufs.workspace, scores=bufs.scores, stream=s)
+        self.step_calls = step_calls
+        self.g_step = capture(step_calls)
+        self.g_score = capture(lambda s: L.locks_score(H, data["q"], summ, data["block_table"], data["seq_lens"],
+                                                       bufs.workspace, scores=bufs.scores, stream=s))
+        self.g_select = capture(lambda s: L.locks_select(H, data["seq_lens"], w.max_pages, w.budget_pages,
+                                                         bufs.selected, bufs.n_selected, bufs.workspace,
+                                                         scores=bufs.scores, stream=s))
+        self.g_sparse = capture(lambda s: L.locks_sparse_decode(
+            H, data["q"], data["k_cache"], data["v_cache"], data["block_table"], data["seq_lens"],
+            bufs.selected, bufs.n_selected, w.budget_pages, bufs.out, bufs.workspace, stream=s))
+        self.g_fused = capture(lambda s: L.locks_select_sparse_decode(
+            H, data["q"], data["k_cache"], data["v_cache"], data["block_table"], data["seq_lens"],
+            w.budget_pages, bufs.selected, bufs.n_selected, bufs.out, bufs.workspace, scores=bufs.scores,
+            stream=s))
+        self.dense_out = torch.empty_like(bufs.out)
+        self.g_dense = capture(lambda s: L.locks_dense_decode(
+            H, data["q"], data["k_cache"], data["v_cache"], data["block_table"], data["seq_lens"],
+            self.dense_out, bufs.workspace, stream=s))
+
+    def fused_path(self, n_sms: int) -> bool:
+        """The library's rule: every (request, KV head) cluster of 8 CTAs
+        resident at once, and at most 32,768 pages of context."""
+        return self.w.batch * self.H * 8 <= n_sms and self.w.max_pages <= 32768
+
+    def measure(self, time_graph, peak: float, n_sms: int, step_us=None):
+        """Per-kernel event times (each graph alone, L2 flushed before each
+        replay) and the roofline entry of every kernel the step launches."""
+        from sparse_long_context_locks_gb300 import workload as W
+        w, H = self.w, self.H
+        lens = self.data["seq_lens"].cpu().tolist()
+        by = W.algorithmic_bytes(lens, H, w.group, w.budget_pages)
+        page_heads = H * sum(L_b // 16 for L_b in lens)
+        io = by["step"] - by["score"] - by["sparse_kv"]
+        us = {"score": time_graph(self.g_score), "fused": time_graph(self.g_fused),
+              "select": time_graph(self.g_select), "sparse": time_graph(self.g_sparse),
+              "dense": time_graph(self.g_dense, reps=10)}
+        if step_us is None:
+            step_us = time_graph(self.g_step)
+        fused = self.fused_path(n_sms)
+
+        def entry(kernel, nbytes, t_us):
+            gbs = nbytes / (t_us * 1e-6) / 1e9
+            return {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                    "frac": gbs / peak, "traffic": measured_traffic(kernel, w.name),
+                    "algorithmic_bytes_per_launch": nbytes, "us": t_us}
+
+        # algorithmic bytes per launch: records (784 B a full page-head) for the
+        # scorer; the scores (16 B a page-head) for the selection; the selected
+        # pages' K and V, the tail tokens, q and out for the attention
+        kernels = [entry("score_kernel", by["score"], us["score"])]
+        if fused:
+            kernels.append(entry("select_attend_kernel", by["sparse_kv"] + 16 * page_heads + io, us["fused"]))
+        else:
+            kernels.append(entry("select_kernel", 16 * page_heads, us["select"]))
+            kernels.append(entry("attn_kernel", by["sparse_kv"] + io, us["sparse"]))
+        step_gbs = by["step"] / (step_us * 1e-6) / 1e9
+        rows = {
+            "step_path": "score + fused select/attend" if fused else "score + select + split-K attend",
+            "step_us": step_us, "tokens_per_s": w.batch / (step_us * 1e-6),
+            "step_GBps": step_gbs,
+            "roofline_step": {"achieved": step_gbs, "peak": peak, "unit": "GB/s", "frac": step_gbs / peak,
+                              "algorithmic_bytes": by["step"]},
+            "score_us": us["score"], "score_frac": kernels[0]["frac"],
+            "select_attend_fused_us": us["fused"], "select_us": us["select"],
+            "sparse_attention_us": us["sparse"],
+            "sparse_attention_GBps": (by["sparse_kv"] + io) / (us["sparse"] * 1e-6) / 1e9,
+            "sparse_attention_frac": (by["sparse_kv"] + io) / (us["sparse"] * 1e-6) / 1e9 / peak,
+            "dense_us": us["dense"], "dense_GBps": by["dense_kv"] / (us["dense"] * 1e-6) / 1e9,
+            "dense_frac": by["dense_kv"] / (us["dense"] * 1e-6) / 1e9 / peak,
+            "bytes_step": by["step"], "bytes_dense": by["dense_step"],
+            "bytes_ratio_dense_over_step": by["dense_step"] / by["step"],
+            "latency_ratio_dense_over_step": us["dense"] / step_us,
+        }
+        return rows, kernels
+
+
 # ------------------------------------------------------------------ main arm
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -256,8 +386,6 @@ def main():
     w = W.CONFIGS[args.workload]
     H, G, B = w.num_kv_heads, w.group, w.batch
     data = W.generate(w.scaled(seed=w.seed + 7919 * rank), device="cuda")
-    lens = data["seq_lens"].cpu().tolist()
-    by = W.algorithmic_bytes(lens, H, G, w.budget_pages)
     summ = torch.zeros(data["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
     blocks = W.full_page_blocks(data).cuda()
     bufs = L.DecodeBuffers(H, B, w.max_pages, w.budget_pages)
@@ -307,10 +435,8 @@ def main():
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda").fill_(1.0)
     sink = torch.zeros((), device="cuda")
 
-    def step_calls(s):
-        L.locks_decode_step(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
-                            data["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
-                            bufs.workspace, scores=bufs.scores, stream=s)
+    def flush_l2():
+        torch.sum(flush, dim=0, out=sink)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -322,27 +448,26 @@ def main():
         torch.cuda.synchronize()
         return g
 
-    g_step = capture(step_calls)
-    g_score = capture(lambda s: L.locks_score(H, data["q"], summ, data["block_table"], data["seq_lens"],
-                                              bufs.workspace, scores=bufs.scores, stream=s))
-    g_select = capture(lambda s: L.locks_select(H, data["seq_lens"], w.max_pages, w.budget_pages,
-                                                bufs.selected, bufs.n_selected, bufs.workspace,
-                                                scores=bufs.scores, stream=s))
-    g_sparse = capture(lambda s: L.locks_sparse_decode(H, data["q"], data["k_cache"], data["v_cache"],
-                                                       data["block_table"], data["seq_lens"], bufs.selected,
-                                                       bufs.n_selected, w.budget_pages, bufs.out,
-                                                       bufs.workspace, stream=s))
-    g_fused = capture(lambda s: L.locks_select_sparse_decode(
-        H, data["q"], data["k_cache"], data["v_cache"], data["block_table"], data["seq_lens"],
-        w.budget_pages, bufs.selected, bufs.n_selected, bufs.out, bufs.workspace, scores=bufs.scores,
-        stream=s))
-    dense_out = torch.empty_like(bufs.out)
-    g_dense = capture(lambda s: L.locks_dense_decode(H, data["q"], data["k_cache"], data["v_cache"],
-                                                     data["block_table"], data["seq_lens"], dense_out,
-                                                     bufs.workspace, stream=s))
+    R = min(200, max(20, args.steps // 10))
 
-    def flush_l2():
-        torch.sum(flush, dim=0, out=sink)
+    def time_graph(g, reps=R, sleep_cycles=400_000):
+        """Mean device time of one replay, L2 flushed before each (outside the
+        events), with the host ahead of the GPU (a sleep kernel before each)."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                flush_l2()
+                torch.cuda._sleep(sleep_cycles)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+        return tot / reps * 1e3   # us
+
+    case = WorkloadCase(L, w, data, summ, bufs, capture)
+    g_step = case.g_step
 
     # ---------------------------------------------------------------- timed steps
     with torch.cuda.stream(stream):
@@ -394,38 +519,18 @@ def main():
                               "clocks": ClockSampler.summary(clock_rows)}))
         return
 
-    # locks_decode_step runs the fused cluster kernel when every (request, KV
-    # head) cluster of 8 CTAs fits on the GPU at once, else selection + split-K
+    peak, peak_src = peaks()
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
-    # the library's rule: every (request, KV head) cluster of 8 CTAs resident
-    # at once, and at most 32,768 pages of context
-    fused_path = B * H * 8 <= n_sms and w.max_pages <= 32768
-    launches_per_step = 2 if fused_path else 3
-    config["step_path"] = "score + fused select/attend" if fused_path else "score + select + split-K attend"
 
     # ---------------------------------------------------------------- per-kernel rows
-    R = min(200, max(20, K // 10))
+    main_rows, kernels = case.measure(time_graph, peak, n_sms, step_us=ms_step * 1e3)
+    launches_per_step = len(kernels)
+    dominant = max(kernels, key=lambda k: k["us"])
+    roofline = dict(dominant, peak_source=peak_src)
 
-    def time_graph(g, reps=R, sleep_cycles=400_000):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        tot = 0.0
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                flush_l2()
-                torch.cuda._sleep(sleep_cycles)
-                e0.record(stream)
-                g.replay()
-                e1.record(stream)
-                e1.synchronize()
-                tot += e0.elapsed_time(e1)
-        return tot / reps * 1e3   # us
-
-    us_score = time_graph(g_score)
-    us_fused = time_graph(g_fused)
-    us_select = time_graph(g_select)
-    us_sparse = time_graph(g_sparse)
-    us_dense = time_graph(g_dense, reps=max(10, R // 4))
     # builder over every full page (prefill-style), timed the same way
+    blocks = W.full_page_blocks(data).cuda()
+
     def build_all(s):
         L.locks_build_summaries(H, data["k_cache"], blocks, summ, bufs.workspace, stream=s)
     g_build = capture(build_all)
@@ -441,20 +546,15 @@ def main():
 
     def crossing_step(s):
         L.locks_build_pending(H, data["k_cache"], pend_ids, n_pend, summ, bufs.workspace, stream=s)
-        step_calls(s)
+        case.step_calls(s)
     g_cross = capture(crossing_step)
     us_cross = time_graph(g_cross)
-
-    peak, peak_src = peaks()
-    score_gbs = by["score"] / (us_score * 1e-6) / 1e9
-    traffic = None
-    try:
-        with open(PROFILE_SUMMARY) as f:
-            prof = json.load(f)
-        if prof.get("source_sha256_16") == score_source_hash() and prof.get("workload") == w.name:
-            traffic = prof.get("dram_bytes_per_launch")
-    except Exception:
-        traffic = None
+    main_rows.update({
+        "build_us": us_build, "build_page_heads": n_page_heads,
+        "build_GBps": (n_page_heads * (4096 + 784)) / (us_build * 1e-6) / 1e9,
+        "build_pending_us": us_pend, "build_pending_page_heads": int(pend_ids.numel()) * H,
+        "step_with_page_crossing_us": us_cross,
+    })
 
     # ---------------------------------------------------------------- e2e
     q_host = data["q"].cpu().pin_memory()
@@ -467,7 +567,7 @@ def main():
         # C ABI, its output back to pinned host memory: one graph
         data["q"].copy_(q_host, non_blocking=True)
         data["seq_lens"].copy_(lens_host, non_blocking=True)
-        step_calls(s)
+        case.step_calls(s)
         out_host.copy_(bufs.out, non_blocking=True)
 
     g_e2e = capture(e2e_calls)
@@ -507,6 +607,28 @@ def main():
                "ms_per_step": cpu_step * 1e3}
         pool.close()
 
+    # ---------------------------------------------------------------- other workloads
+    # the same per-kernel rows on the other single-GPU workloads, in this run
+    # (the headline workload's buffers are released first)
+    others = {}
+    extra = [x for x in args.extra_workloads.split(",") if x and x != w.name] if rank == 0 else []
+    if extra:
+        del case, g_step, g_build, g_pend, g_cross, g_e2e, data, summ, bufs, blocks
+        torch.cuda.empty_cache()
+    for name in extra:
+        wx = W.CONFIGS[name]
+        dx = W.generate(wx, device="cuda")
+        sx = torch.zeros(dx["num_blocks"], wx.num_kv_heads, 784, dtype=torch.uint8, device="cuda")
+        bx = L.DecodeBuffers(wx.num_kv_heads, wx.batch, wx.max_pages, wx.budget_pages)
+        L.locks_build_summaries(wx.num_kv_heads, dx["k_cache"], W.full_page_blocks(dx).cuda(), sx,
+                                bx.workspace)
+        cx = WorkloadCase(L, wx, dx, sx, bx, capture)
+        rows_x, kern_x = cx.measure(time_graph, peak, n_sms, step_us=None)
+        rows_x["status_flags"] = L.locks_read_status(bx.workspace)
+        others[name] = {"rows": rows_x, "roofline_kernels": kern_x}
+        del cx, dx, sx, bx
+        torch.cuda.empty_cache()
+
     if rank != 0:
         return
     line = {
@@ -514,6 +636,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": config,
+        "step_path": main_rows["step_path"],
         "clocks": ClockSampler.summary(clock_rows),
         "e2e": {"value": w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -521,25 +644,11 @@ def main():
                         "seq_lens, locks_decode_step and the D2H copy of out, then a stream sync; L2 "
                         "flushed before each step, outside the timed window"},
         "gpu_launches": launches_per_step * K,
-        "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs, "peak": peak,
-                     "unit": "GB/s", "frac": score_gbs / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": by["score"], "peak_source": peak_src},
-        "rows": {
-            "score_us": us_score, "select_attend_fused_us": us_fused,
-            "select_us": us_select, "sparse_attention_us": us_sparse,
-            "step_us": ms_step * 1e3,
-            "step_GBps": by["step"] / (ms_step * 1e-3) / 1e9,
-            "sparse_attention_GBps": by["sparse_kv"] / (us_sparse * 1e-6) / 1e9,
-            "dense_us": us_dense, "dense_GBps": by["dense_kv"] / (us_dense * 1e-6) / 1e9,
-            "dense_frac": by["dense_kv"] / (us_dense * 1e-6) / 1e9 / peak,
-            "build_us": us_build, "build_page_heads": n_page_heads,
-            "build_pending_us": us_pend, "build_pending_page_heads": int(pend_ids.numel()) * H,
-            "step_with_page_crossing_us": us_cross,
-            "build_GBps": (n_page_heads * (4096 + 784)) / (us_build * 1e-6) / 1e9,
-            "bytes_step": by["step"], "bytes_dense": by["dense_step"],
-            "bytes_ratio_dense_over_step": by["dense_step"] / by["step"],
-            "latency_ratio_dense_over_step": us_dense / (ms_step * 1e3),
-        },
+        "roofline": roofline,
+        "roofline_kernels": kernels,
+        "roofline_step": main_rows["roofline_step"],
+        "rows": main_rows,
+        "workloads": others,
         "cpu_baseline": cpu,
         "status_flags": status,
         "wall_timed_s": t_wall,

@@ -12,9 +12,11 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-def _line(sm, mx, power, hw="Not Active", hw_th="Not Active", sw_th="Not Active", sw_pw="Not Active"):
-    # --query-gpu=timestamp,index,clocks.sm,clocks.max.sm,power.draw,active,hw,hw_thermal,sw_thermal,sw_power
-    return f"2026/12/03 01:00:00.000, 0, {sm}, {mx}, {power}, 0x0, {hw}, {hw_th}, {sw_th}, {sw_pw}\n"
+def _line(sm, mx, power, util=100, hw="Not Active", hw_th="Not Active", sw_th="Not Active",
+          sw_pw="Not Active"):
+    # --query-gpu=timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,active,
+    #             hw,hw_thermal,sw_thermal,sw_power   (--format=csv,noheader,nounits)
+    return f"2026/12/03 01:00:00.000, 0, {sm}, {mx}, {power}, {util}, 0x0, {hw}, {hw_th}, {sw_th}, {sw_pw}\n"
 
 
 def _parse(lines):
@@ -27,23 +29,32 @@ def _parse(lines):
 def test_rows_parsed_and_malformed_lines_skipped():
     rows = _parse([_line(2070, 2070, 900.5), "garbage\n", _line("[N/A]", 2070, 10.0), _line(1980, 2070, 1200)])
     assert [r["sm"] for r in rows] == [2070.0, 1980.0]
-    assert rows[1]["power"] == 1200.0 and rows[0]["max"] == 2070.0
+    assert rows[1]["power"] == 1200.0 and rows[0]["max"] == 2070.0 and rows[0]["util"] == 100.0
 
 
 def test_summary_median_max_and_active_reasons():
     rows = _parse([_line(2070, 2070, 800), _line(1800, 2070, 1300, sw_pw="Active"),
-                   _line(2070, 2070, 900), _line(1500, 2100, 1400, hw_th="Active"),
-                   _line(2070, 2070, 0.0)])   # idle sample: not under load, left out
+                   _line(2070, 2070, 900, util=97), _line(1500, 2100, 1400, hw_th="Active"),
+                   _line(345, 2070, 120.0, util=0),            # idle samples: not under load
+                   _line(1000, 2070, 300.0, util=12, sw_th="Active")])
     s = bench.ClockSampler.summary(rows)
-    assert s["samples"] == 4
+    assert s["samples"] == 6 and s["samples_under_load"] == 4
     assert s["sm_mhz"] == 2070.0          # upper median of 1500, 1800, 2070, 2070
     assert s["sm_max_mhz"] == 2100.0
-    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]   # the idle sample's is left out
+
+
+def test_summary_with_no_sample_under_load_uses_all():
+    rows = _parse([_line(345, 2070, 120.0, util=0), _line(400, 2070, 130.0, util=3)])
+    s = bench.ClockSampler.summary(rows)
+    assert s["samples"] == 2 and s["samples_under_load"] == 0
+    assert s["sm_mhz"] == 400.0
 
 
 def test_summary_without_samples_says_so():
     s = bench.ClockSampler.summary([])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["reasons"] == ["no samples"]
+    assert s["samples_under_load"] == 0
 
 
 def test_cpu_baseline_unit_runs_the_whole_oracle_path(tmp_path):
