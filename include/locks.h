@@ -29,8 +29,12 @@
  *    locks_read_status() returns it (that call synchronises `stream`).
  *    Every wait on an mbarrier is bounded (about one second of %globaltimer);
  *    when one runs out the kernel flags LOCKS_FLAG_TIMEOUT and returns.
- *  - Fixed shape: head_dim d = 128, page_size B = 16, rank r = 8, quantised
- *    summaries; group_size G = 4.  Other values return LOCKS_ERR_UNSUPPORTED.
+ *  - Fixed shape: head_dim d = 128, page_size B = 16, group_size G = 4, and
+ *    either quantised summaries at rank r = 8 (quant = 1, the method's
+ *    records) or unquantised fp32 summaries of rank 1 <= r <= 16 (quant = 0,
+ *    a debug and reference configuration: at r = 16 a record reproduces its
+ *    page's keys exactly, so s_j is the exact page log-sum-exp).  Other
+ *    values return LOCKS_ERR_UNSUPPORTED.
  *
  * Tensor layouts
  * --------------
@@ -77,6 +81,11 @@
  *             sum_{k>8} lambda_k (diagnostic of §3 Thm. 1; not used by scoring).
  *  The byte map puts each lane's share of a tensor-core fragment in one
  *  contiguous 16/32/4-byte run, so the scorer loads it with single vector loads.
+ *
+ * Unquantised record (quant = 0, rank r): 528 + 576 r bytes per page-head,
+ * fp32 little-endian: [mu: 128][V: 128 x r, V[dim][k] at dim * r + k]
+ * [C: 16 x r, c[i][k] at i * r + k][tail energy sum_{k>r} lambda_k, 0, 0, 0];
+ * the same centroid, eigenpairs, ranking, sign and zero-floor rules.
  */
 #ifndef LOCKS_H
 #define LOCKS_H
@@ -104,10 +113,10 @@ typedef enum {
 typedef struct {
   int32_t head_dim;      /* d: 128 */
   int32_t page_size;     /* B: 16 */
-  int32_t rank;          /* r: 8 */
+  int32_t rank;          /* r: 8 (quant = 1) or 1..16 (quant = 0) */
   int32_t num_kv_heads;  /* H_kv >= 1 */
   int32_t group_size;    /* G: 4 query heads per KV head */
-  int32_t quant;         /* 1: int4 basis, int8 centroid/coefficients */
+  int32_t quant;         /* 1: int4 basis, int8 centroid/coefficients; 0: fp32 */
 } locks_cfg;
 
 /* Status-word bits written by the kernels (see locks_read_status). */
@@ -116,8 +125,8 @@ typedef struct {
 #define LOCKS_FLAG_TIMEOUT     4u  /* a bounded wait on an mbarrier ran out */
 #define LOCKS_FLAG_BAD_SELECT  8u  /* a selected index outside [0, n_b) was skipped */
 
-/* Bytes of one page-head summary record (784 for the supported shape),
- * 0 for an unsupported cfg. */
+/* Bytes of one page-head summary record (784 for quant = 1, 528 + 576 r for
+ * quant = 0), 0 for an unsupported cfg. */
 size_t locks_summary_bytes(const locks_cfg *cfg);
 
 /* Workspace bytes needed by score/select and sparse/dense decode for this
@@ -262,6 +271,95 @@ locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void 
                                 const int32_t *block_table, const int32_t *seq_lens,
                                 int32_t batch, int32_t max_pages, float sm_scale, float *out,
                                 void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Shared-basis ablation, §3 "impossibility of shared projections": the
+ * comparison selector the method is measured against, which scores every page
+ * of a KV head through ONE rank-rho basis U (fp32 [H_kv][128][rho], the
+ * caller's, e.g. the top principal directions of the head's centred keys;
+ * 1 <= rho <= 64) instead of each page's own.  Record per page-head, fp32,
+ * 512 + 64 rho bytes: [mu: 128][c: 16 x rho, c[i][k] = U[:,k].(k_i - mu)].
+ * Score: s_j = log sum_i exp((q.mu + (U^T q).c_i) / sqrt(d)), written to the
+ * same table as locks_score's, so locks_select and locks_sparse_decode run on
+ * it unchanged.  Block ids outside the cache are flagged and skipped.
+ * ------------------------------------------------------------------------ */
+locks_status locks_shared_basis_build(const locks_cfg *cfg, const void *k_cache, int64_t num_blocks,
+                                      const int32_t *block_ids, int32_t n_build, const float *basis, int32_t rho,
+                                      void *records, void *workspace, size_t workspace_bytes,
+                                      locks_stream_t stream);
+
+locks_status locks_shared_basis_score(const locks_cfg *cfg, const void *q, const float *basis, int32_t rho,
+                                      const void *records, int64_t num_blocks, const int32_t *block_table,
+                                      const int32_t *seq_lens, int32_t batch, int32_t max_pages, float *scores,
+                                      void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Context-parallel shards: one request's full pages split over several GPUs.
+ *
+ * §2 "Reconstruction and selection" / "Group-shared selection (GQA)" normalise
+ * each query head's page scores over all of a request's pages, and §4 places
+ * the method at 1M+ token contexts.  When a request's pages are split over
+ * n_shards GPUs (shard r holds the contiguous logical pages starting at
+ * page_offset[b]; only the last shard may hold the open tail page), each shard
+ * runs the calls below on its own cache and block table, with shard_lens[b]
+ * its own token count in place of seq_lens.  Between them the caller gathers
+ * three small results from every shard (an all-gather over any transport:
+ * the kernels never wait on another GPU):
+ *   1. locks_score (unchanged), then locks_cp_score_pairs -> pairs
+ *      float [batch][H_kv][G][2];  gather -> pairs_all [n_shards][...];
+ *   2. locks_cp_select_local -> this shard's top-min(budget, n) pages as
+ *      candidates: cand_pages int32 [batch][H_kv][budget] (global page
+ *      indices, ascending), cand_keys uint32 (same shape; the selection key,
+ *      fp32 bits of the page's group-mean share), cand_counts int32
+ *      [batch][H_kv];  gather all three over shards;
+ *   3. locks_cp_merge_select -> the global top-k restricted to this shard
+ *      (local page indices, ascending) in selected / n_selected; then
+ *      locks_cp_sparse_decode_partial -> states float [batch][H_kv*G][130]
+ *      (per query head: m in log2 units, l, unnormalised o[128]);
+ *      gather -> states_all [n_shards][...];  locks_cp_merge_attention -> out.
+ * The selection equals the one-GPU selection up to the rounding of Z_g (keys
+ * are computed by the same code on every shard; ties go to the lower global
+ * page index); the output is attention over the union of the shards'
+ * selected pages plus the tail.  n_shards * budget_pages <= 16384.
+ * ------------------------------------------------------------------------ */
+
+/* Per (request, KV head, query head): max over the shard's full pages of
+ * s_j*log2(e) and the sum of 2^(s_j*log2(e) - max) -> pairs (16-byte aligned).
+ * `scores` as given to locks_score (NULL: the workspace's). */
+locks_status locks_cp_score_pairs(const locks_cfg *cfg, const int32_t *shard_lens, int32_t batch,
+                                  int32_t max_pages, const float *scores, float *pairs, void *workspace,
+                                  size_t workspace_bytes, locks_stream_t stream);
+
+/* The shard's local selection with Z_g from every shard's pairs, written as
+ * candidates (see above).  page_offset: device int32 [batch]. */
+locks_status locks_cp_select_local(const locks_cfg *cfg, const int32_t *shard_lens, const int32_t *page_offset,
+                                   int32_t batch, int32_t max_pages, int32_t budget_pages, const float *scores,
+                                   const float *pairs_all, int32_t n_shards, int32_t *cand_pages,
+                                   uint32_t *cand_keys, int32_t *cand_counts, void *workspace,
+                                   size_t workspace_bytes, locks_stream_t stream);
+
+/* The k = min(budget, total candidates) largest candidates of all shards
+ * (key descending, lower global page first); this shard's share of them as
+ * local page indices, ascending. */
+locks_status locks_cp_merge_select(const locks_cfg *cfg, const int32_t *page_offset, int32_t batch,
+                                   int32_t budget_pages, int32_t n_shards, int32_t shard,
+                                   const int32_t *cand_pages_all, const uint32_t *cand_keys_all,
+                                   const int32_t *cand_counts_all, int32_t *selected, int32_t *n_selected,
+                                   locks_stream_t stream);
+
+/* locks_sparse_decode over the shard's selected pages (and its tail page, if
+ * it holds one), writing the unnormalised state instead of `out`. */
+locks_status locks_cp_sparse_decode_partial(const locks_cfg *cfg, const void *q, const void *k_cache,
+                                            const void *v_cache, int64_t num_blocks, const int32_t *block_table,
+                                            const int32_t *shard_lens, const int32_t *selected,
+                                            const int32_t *n_selected, int32_t batch, int32_t max_pages,
+                                            int32_t budget_pages, float sm_scale, float *states, void *workspace,
+                                            size_t workspace_bytes, locks_stream_t stream);
+
+/* out[b][hq][:] = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r over the
+ * shards' states (zero when every shard's l is zero). */
+locks_status locks_cp_merge_attention(const locks_cfg *cfg, int32_t batch, int32_t n_shards,
+                                      const float *states_all, float *out, locks_stream_t stream);
 
 /* Sparse decode attention without a caller-provided workspace.  The paper
  * has no counterpart: this exists for callers that cannot allocate device

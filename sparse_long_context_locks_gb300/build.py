@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "liblocks.so")
 SOURCES = ["api.cu", "build_summaries.cu", "score_select.cu", "decode_attention.cu", "noalloc.cu",
-           "select_attend.cu", "wait_check.cu"]
+           "select_attend.cu", "wait_check.cu", "context_parallel.cu",
+           "score_debug.cu", "shared_basis.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

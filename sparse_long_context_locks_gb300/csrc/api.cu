@@ -24,8 +24,9 @@ namespace locks {
 
 bool cfg_supported(const locks_cfg* c) {
   if (c == nullptr) return false;
-  if (c->head_dim != kHeadDim || c->page_size != kPage || c->rank != kRank) return false;
-  if (c->quant != 1 || c->group_size != kGroup) return false;
+  if (c->head_dim != kHeadDim || c->page_size != kPage || c->group_size != kGroup) return false;
+  // quantised records at rank 8, or unquantised fp32 records of rank 1..16
+  if (!((c->quant == 1 && c->rank == kRank) || (c->quant == 0 && c->rank >= 1 && c->rank <= kPage))) return false;
   const int H = c->num_kv_heads;
   if (H < 1) return false;
   const int h_cta = H < 8 ? H : 8;
@@ -221,7 +222,7 @@ locks_status attention_common(const locks_cfg* cfg, const void* q, const void* k
                               const int32_t* seq_lens, const int32_t* selected,
                               const int32_t* n_selected, int32_t batch, int32_t max_pages,
                               int32_t budget_pages, float sm_scale, float* out, void* workspace,
-                              size_t ws_bytes, cudaStream_t stream, bool dense) {
+                              size_t ws_bytes, cudaStream_t stream, bool dense, float* state_out = nullptr) {
   if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
   if (batch < 0 || max_pages < 1 || budget_pages < 0 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || sm_scale != sm_scale) return LOCKS_ERR_INVALID_ARG;
@@ -231,7 +232,7 @@ locks_status attention_common(const locks_cfg* cfg, const void* q, const void* k
   LOCKS_CHECK_PTR(v_cache);
   LOCKS_CHECK_PTR(block_table);
   LOCKS_CHECK_PTR(seq_lens);
-  LOCKS_CHECK_PTR(out);
+  if (state_out == nullptr) LOCKS_CHECK_PTR(out);
   LOCKS_CHECK_PTR(workspace);
   if (!dense) {
     LOCKS_CHECK_PTR(n_selected);
@@ -254,6 +255,7 @@ locks_status attention_common(const locks_cfg* cfg, const void* q, const void* k
   p.selected = selected;
   p.n_selected = n_selected;
   p.out = out;
+  p.state_out = state_out;
   p.part = reinterpret_cast<float*>(ws + pl.off_attn);
   p.tickets = reinterpret_cast<uint32_t*>(ws + pl.off_tickets);
   p.status = status_word(workspace);
@@ -273,7 +275,10 @@ locks_status attention_common(const locks_cfg* cfg, const void* q, const void* k
 
 extern "C" {
 
-size_t locks_summary_bytes(const locks_cfg* cfg) { return cfg_supported(cfg) ? (size_t)kRecord : 0; }
+size_t locks_summary_bytes(const locks_cfg* cfg) {
+  if (!cfg_supported(cfg)) return 0;
+  return cfg->quant == 1 ? (size_t)kRecord : (size_t)(528 + 576 * cfg->rank);
+}
 
 locks_status locks_workspace_bytes(const locks_cfg* cfg, int32_t batch, int32_t max_pages,
                                    int32_t budget_pages, size_t* bytes) {
@@ -321,6 +326,7 @@ locks_status locks_build_summaries(const locks_cfg* cfg, const void* k_cache, in
   p.num_blocks = num_blocks;
   p.n_build = n_build;
   p.H_kv = cfg->num_kv_heads;
+  if (cfg->quant == 0) return from_cuda(launch_build_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
   return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -346,6 +352,7 @@ locks_status locks_build_pending(const locks_cfg* cfg, const void* k_cache, int6
   p.num_blocks = num_blocks;
   p.n_build = max_pending;
   p.H_kv = cfg->num_kv_heads;
+  if (cfg->quant == 0) return from_cuda(launch_build_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
   return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -383,6 +390,7 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   p.n_chunks = pl.n_chunks;
   p.head_groups = pl.head_groups;
   p.n_items = pl.n_items;
+  if (cfg->quant == 0) return from_cuda(launch_score_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
   return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -550,6 +558,150 @@ locks_status locks_dense_decode(const locks_cfg* cfg, const void* q, const void*
   return attention_common(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, nullptr, nullptr,
                           batch, max_pages, 0, sm_scale, out, workspace, workspace_bytes,
                           reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+// ---------------------------------------------------------------- shared-basis ablation
+locks_status locks_shared_basis_build(const locks_cfg* cfg, const void* k_cache, int64_t num_blocks,
+                                      const int32_t* block_ids, int32_t n_build, const float* basis, int32_t rho,
+                                      void* records, void* workspace, size_t workspace_bytes,
+                                      locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (n_build < 0 || num_blocks < 1 || rho < 1 || rho > 64) return LOCKS_ERR_INVALID_ARG;
+  if (n_build == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(k_cache);
+  LOCKS_CHECK_PTR(block_ids);
+  LOCKS_CHECK_PTR(basis);
+  LOCKS_CHECK_PTR(records);
+  if (workspace != nullptr && (!aligned16(workspace) || workspace_bytes < sizeof(uint32_t)))
+    return LOCKS_ERR_INVALID_ARG;
+  return from_cuda(launch_shared_basis_build(static_cast<const __nv_bfloat16*>(k_cache), num_blocks, block_ids,
+                                             n_build, cfg->num_kv_heads, basis, rho,
+                                             static_cast<uint8_t*>(records), status_word(workspace),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_shared_basis_score(const locks_cfg* cfg, const void* q, const float* basis, int32_t rho,
+                                      const void* records, int64_t num_blocks, const int32_t* block_table,
+                                      const int32_t* seq_lens, int32_t batch, int32_t max_pages, float* scores,
+                                      void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || num_blocks < 1 || rho < 1 || rho > 64) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(q);
+  LOCKS_CHECK_PTR(basis);
+  LOCKS_CHECK_PTR(records);
+  LOCKS_CHECK_PTR(block_table);
+  LOCKS_CHECK_PTR(seq_lens);
+  LOCKS_CHECK_PTR(workspace);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  const Plan pl = make_plan(cfg, batch, max_pages, 0);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  float* sc = scores ? scores : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.off_scores);
+  return from_cuda(launch_shared_basis_score(static_cast<const __nv_bfloat16*>(q), basis, rho,
+                                             static_cast<const uint8_t*>(records), num_blocks, block_table, seq_lens,
+                                             batch, cfg->num_kv_heads, max_pages, sc, status_word(workspace),
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- context-parallel shards
+locks_status locks_cp_score_pairs(const locks_cfg* cfg, const int32_t* shard_lens, int32_t batch, int32_t max_pages,
+                                  const float* scores, float* pairs, void* workspace, size_t workspace_bytes,
+                                  locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(shard_lens);
+  LOCKS_CHECK_PTR(pairs);
+  LOCKS_CHECK_PTR(workspace);
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  const Plan pl = make_plan(cfg, batch, max_pages, 0);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  const float* sc = scores ? scores : reinterpret_cast<const float*>(static_cast<uint8_t*>(workspace) + pl.off_scores);
+  return from_cuda(launch_cp_pairs(shard_lens, sc, pairs, status_word(workspace), batch * cfg->num_kv_heads,
+                                   cfg->num_kv_heads, max_pages, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_cp_select_local(const locks_cfg* cfg, const int32_t* shard_lens, const int32_t* page_offset,
+                                   int32_t batch, int32_t max_pages, int32_t budget_pages, const float* scores,
+                                   const float* pairs_all, int32_t n_shards, int32_t* cand_pages, uint32_t* cand_keys,
+                                   int32_t* cand_counts, void* workspace, size_t workspace_bytes,
+                                   locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || max_pages < 1 || budget_pages < 0 || n_shards < 1) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(shard_lens);
+  LOCKS_CHECK_PTR(page_offset);
+  LOCKS_CHECK_PTR(pairs_all);
+  LOCKS_CHECK_PTR(cand_counts);
+  LOCKS_CHECK_PTR(workspace);
+  if (budget_pages > 0) {
+    LOCKS_CHECK_PTR(cand_pages);
+    LOCKS_CHECK_PTR(cand_keys);
+  }
+  if (scores != nullptr && !aligned16(scores)) return LOCKS_ERR_INVALID_ARG;
+  if (!cp_merge_fits(n_shards, budget_pages)) return LOCKS_ERR_UNSUPPORTED;
+  if ((max_pages + kSelCluster - 1) / kSelCluster > kFusedMaxKeysPerCta ||
+      select_smem_bytes(max_pages, budget_pages) > (size_t)kSmemLimit)
+    return LOCKS_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(cfg, batch, max_pages, budget_pages);
+  if (workspace_bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  SelectParams p{};
+  fill_select(p, pl, cfg, shard_lens, batch, max_pages, budget_pages, scores, cand_pages, cand_counts, workspace);
+  p.zpairs = pairs_all;
+  p.z_shards = n_shards;
+  const int units = batch * cfg->num_kv_heads;
+  const int cluster = select_cluster(units, max_pages, budget_pages);
+  p.stage_scores = 0;
+  cudaError_t e = launch_select(p, units, cluster, s);
+  if (e != cudaSuccess || budget_pages == 0) return from_cuda(e);
+  return from_cuda(launch_cp_candidates(p.scores, pairs_all, n_shards, page_offset, cand_pages, cand_keys,
+                                        cand_counts, units, cfg->num_kv_heads, max_pages, budget_pages, s));
+}
+
+locks_status locks_cp_merge_select(const locks_cfg* cfg, const int32_t* page_offset, int32_t batch,
+                                   int32_t budget_pages, int32_t n_shards, int32_t shard,
+                                   const int32_t* cand_pages_all, const uint32_t* cand_keys_all,
+                                   const int32_t* cand_counts_all, int32_t* selected, int32_t* n_selected,
+                                   locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || budget_pages < 0 || n_shards < 1 || shard < 0 || shard >= n_shards) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  if (!cp_merge_fits(n_shards, budget_pages)) return LOCKS_ERR_UNSUPPORTED;
+  LOCKS_CHECK_PTR(page_offset);
+  LOCKS_CHECK_PTR(cand_counts_all);
+  LOCKS_CHECK_PTR(n_selected);
+  if (budget_pages > 0) {
+    LOCKS_CHECK_PTR(cand_pages_all);
+    LOCKS_CHECK_PTR(cand_keys_all);
+    LOCKS_CHECK_PTR(selected);
+  }
+  return from_cuda(launch_cp_merge_select(cand_pages_all, cand_keys_all, cand_counts_all, n_shards, shard,
+                                          page_offset, selected, n_selected, batch * cfg->num_kv_heads,
+                                          cfg->num_kv_heads, budget_pages, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+locks_status locks_cp_sparse_decode_partial(const locks_cfg* cfg, const void* q, const void* k_cache,
+                                            const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                                            const int32_t* shard_lens, const int32_t* selected,
+                                            const int32_t* n_selected, int32_t batch, int32_t max_pages,
+                                            int32_t budget_pages, float sm_scale, float* states, void* workspace,
+                                            size_t workspace_bytes, locks_stream_t stream) {
+  if (states == nullptr || !aligned16(states)) return LOCKS_ERR_INVALID_ARG;
+  return attention_common(cfg, q, k_cache, v_cache, num_blocks, block_table, shard_lens, selected, n_selected,
+                          batch, max_pages, budget_pages, sm_scale, nullptr, workspace, workspace_bytes,
+                          reinterpret_cast<cudaStream_t>(stream), false, states);
+}
+
+locks_status locks_cp_merge_attention(const locks_cfg* cfg, int32_t batch, int32_t n_shards, const float* states_all,
+                                      float* out, locks_stream_t stream) {
+  if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
+  if (batch < 0 || n_shards < 1) return LOCKS_ERR_INVALID_ARG;
+  if (batch == 0) return LOCKS_OK;
+  LOCKS_CHECK_PTR(states_all);
+  LOCKS_CHECK_PTR(out);
+  return from_cuda(launch_cp_merge_attn(states_all, n_shards, batch * cfg->num_kv_heads * kGroup, out,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* locks_status_str(locks_status s) {

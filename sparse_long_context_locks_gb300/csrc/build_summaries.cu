@@ -121,31 +121,14 @@ struct Sweep<15> {
   static __device__ __forceinline__ void run(float (&)[kPage], float (&)[kPage], int, int, HalfWarpSmem&) {}
 };
 
-__global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams p) {
-  extern __shared__ __align__(16) uint8_t smem_b[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, i = lane & 15, hbase = lane & 16;
-  HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_b)[warp * 2 + half];
-
-  const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;   // page-head index
-  const int n_pages = p.n_dev != nullptr ? min(p.n_build, max(0, *p.n_dev)) : p.n_build;
-  const int64_t total = (int64_t)n_pages * p.H_kv;
-  bool active = ph < total;
-  int64_t blk = -1;
-  int h = 0;
-  if (active) {
-    blk = p.block_ids[ph / p.H_kv];
-    h = (int)(ph % p.H_kv);
-    if (blk < 0 || blk >= p.num_blocks) {
-      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
-      active = false;
-    }
-  }
-  // Both half-warps run every step (warp-synchronous shuffles); an inactive
-  // half works on a zero page and stores nothing.
-
+// Steps 1-3 for the half-warp's page-head (block blk, KV head h; a zero page
+// when !active): lane i ends with the centroid of dims 8i..8i+7 in mu8, row i
+// of the rotated Gram matrix in g (its diagonal: the eigenvalues, also in
+// S.G) and row i of the eigenvector matrix in w; S.X holds the centred keys.
+__device__ __forceinline__ void build_eigen(const BuildParams& p, HalfWarpSmem& S, bool active, int64_t blk, int h,
+                                            int i, int hbase, float (&mu8)[8], float (&g)[kPage],
+                                            float (&w)[kPage]) {
   // ---- 1. load, centroid, centred rows
-  float mu8[8];
   {
     float kv[kPage][8];
     const __nv_bfloat16* src = p.k_cache + ((active ? blk : 0) * p.H_kv + h) * (int64_t)(kPage * kHeadDim);
@@ -177,7 +160,6 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   __syncwarp();
 
   // ---- 2. Gram row i
-  float g[kPage];
 #pragma unroll
   for (int j = 0; j < kPage; ++j) g[j] = 0.f;
   for (int d = 0; d < kHeadDim; d += 4) {
@@ -191,7 +173,6 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
       g[j] = fmaf(xi.w, xj.w, g[j]);
     }
   }
-  float w[kPage];
 #pragma unroll
   for (int j = 0; j < kPage; ++j) w[j] = (j == i) ? 1.f : 0.f;
 #pragma unroll
@@ -204,6 +185,41 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // eigenvalues coupled; in fp32 the top-8 directions reach their rounding
   // floor after 7 sweeps on low-rank, noisy and full-rank pages alike.
   for (int sweep = 0; sweep < kSweeps; ++sweep) Sweep<0>::run(g, w, i, hbase, S);
+}
+
+// The half-warp's page-head of this launch: its block and KV head, and
+// whether it is built (a block id outside the cache is flagged and skipped).
+__device__ __forceinline__ bool build_target(const BuildParams& p, int i, int64_t& blk, int& h) {
+  const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1;
+  const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;   // page-head index
+  const int n_pages = p.n_dev != nullptr ? min(p.n_build, max(0, *p.n_dev)) : p.n_build;
+  const int64_t total = (int64_t)n_pages * p.H_kv;
+  bool active = ph < total;
+  blk = -1;
+  h = 0;
+  if (active) {
+    blk = p.block_ids[ph / p.H_kv];
+    h = (int)(ph % p.H_kv);
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+      active = false;
+    }
+  }
+  return active;
+}
+
+__global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams p) {
+  extern __shared__ __align__(16) uint8_t smem_b[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, i = lane & 15, hbase = lane & 16;
+  HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_b)[warp * 2 + half];
+  int64_t blk;
+  int h;
+  // Both half-warps run every step (warp-synchronous shuffles); an inactive
+  // half works on a zero page and stores nothing.
+  const bool active = build_target(p, i, blk, h);
+  float mu8[8], g[kPage], w[kPage];
+  build_eigen(p, S, active, blk, h, i, hbase, mu8, g, w);
 
   // ---- 4. rank eigenvalues, pick the top r, fix signs
 #pragma unroll
@@ -354,6 +370,115 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     const uint4* srcr = reinterpret_cast<const uint4*>(S.rec);
     for (int c = i; c < kRecord / 16; c += 16) dst[c] = srcr[c];
   }
+}
+
+// ---------------------------------------------------------------- fp32 records
+// Unquantised records of rank r <= 16 (cfg quant = 0, a debug and reference
+// configuration): the same centroid, Gram matrix and Jacobi eigenpairs, the
+// top r directions (same ranking, sign and zero-floor rules), written as fp32
+// [mu: 128][V: 128 x r, dim-major][C: 16 x r][tail energy, 0, 0, 0].
+struct DebugLift {
+  float lift[kPage * kPage];   // [token][direction]: W_r Lambda^{-1/2}
+  float coef[kPage * kPage];   // [token][direction]: C
+};
+constexpr int kDebugSmem = 2 * kBuildWarps * (int)(sizeof(HalfWarpSmem) + sizeof(DebugLift));
+
+__global__ void __launch_bounds__(kBuildThreads) build_debug_kernel(const BuildParams p, int rank_r) {
+  extern __shared__ __align__(16) uint8_t smem_d[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, i = lane & 15, hbase = lane & 16;
+  HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_d)[warp * 2 + half];
+  DebugLift& D = reinterpret_cast<DebugLift*>(smem_d + 2 * kBuildWarps * sizeof(HalfWarpSmem))[warp * 2 + half];
+  int64_t blk;
+  int h;
+  const bool active = build_target(p, i, blk, h);
+  float mu8[8], g[kPage], w[kPage];
+  build_eigen(p, S, active, blk, h, i, hbase, mu8, g, w);
+
+#pragma unroll
+  for (int j = 0; j < kPage; j += 4)
+    *reinterpret_cast<float4*>(&S.W[i * kPage + j]) = make_float4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+  __syncwarp();
+  float lam[kPage];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) {
+    const float v = S.G[j * kPage + j];
+    lam[j] = v == v ? v : -INFINITY;
+  }
+  const float my_lam = lam[i];
+  int pos = 0;
+  float lam1 = lam[0];
+#pragma unroll
+  for (int j = 0; j < kPage; ++j) {
+    pos += (lam[j] > my_lam) || (lam[j] == my_lam && j < i);
+    lam1 = fmaxf(lam1, lam[j]);
+  }
+  S.order[pos] = i;
+  float tail = pos >= rank_r ? fmaxf(my_lam, 0.f) : 0.f;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) tail += __shfl_xor_sync(0xffffffffu, tail, o);
+  __syncwarp();
+  {
+    // lane i: direction i (when i < r)
+    const int ev = S.order[i];
+    const float l = S.G[ev * kPage + ev];
+    const bool keep = i < rank_r && l > 1e-6f * lam1 && l > 0.f;
+    float best = -1.f, sgn = 1.f;
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      const float v = S.W[r * kPage + ev];
+      if (fabsf(v) > best) {
+        best = fabsf(v);
+        sgn = v < 0.f ? -1.f : 1.f;
+      }
+    }
+    const float sig = keep ? sqrtf(l) : 0.f;
+    const float inv = keep ? 1.f / sig : 0.f;
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      const float v = S.W[r * kPage + ev] * sgn;
+      D.lift[r * kPage + i] = v * inv;
+      D.coef[r * kPage + i] = v * sig;
+    }
+  }
+  __syncwarp();
+  if (!active) return;
+  float* rec = reinterpret_cast<float*>(p.summ + (blk * p.H_kv + h) * (int64_t)(528 + 576 * rank_r));
+  // centroid
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rec[8 * i + e] = mu8[e];
+  // V rows of dims 8i..8i+7: V[dim][k] = sum_r X[r][dim] lift[r][k]
+  float* Vd = rec + kHeadDim;
+  for (int k = 0; k < rank_r; ++k) {
+    float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kPage; ++r) {
+      const float lk = D.lift[r * kPage + k];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v8[e] = fmaf(S.X[r * kXStride + 8 * i + e], lk, v8[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Vd[(8 * i + e) * rank_r + k] = v8[e];
+  }
+  // C row of token i
+  float* Cd = Vd + kHeadDim * rank_r;
+  for (int k = 0; k < rank_r; ++k) Cd[i * rank_r + k] = D.coef[i * kPage + k];
+  if (i == 0) {
+    float* t = Cd + kPage * rank_r;
+    t[0] = tail;
+    t[1] = t[2] = t[3] = 0.f;
+  }
+}
+
+cudaError_t launch_build_debug(const BuildParams& p, int rank_r, cudaStream_t stream) {
+  static DynSmemAttr smem_attr;
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(build_debug_kernel), kDebugSmem, smem_attr);
+  if (e != cudaSuccess) return e;
+  const int64_t page_heads = (int64_t)p.n_build * p.H_kv;
+  const int64_t grid = (page_heads + 2 * kBuildWarps - 1) / (2 * kBuildWarps);
+  if (grid == 0) return cudaSuccess;
+  build_debug_kernel<<<(unsigned)grid, kBuildThreads, kDebugSmem, stream>>>(p, rank_r);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream) {

@@ -120,6 +120,31 @@ __device__ __forceinline__ uint32_t lvl_digit(uint32_t key, int lvl) {
   return (key >> lvl_shift(lvl)) & ((1u << lvl_bits(lvl)) - 1u);
 }
 
+// Selection key of one page: the mean over the group's heads of the page's
+// mass share exp(s_g - Z_g), computed in log2 units (z = log2 Z_g), as fp32
+// bits (non-negative floats order like unsigned ints).  A non-finite or
+// negative mean becomes 0.  Every selection path takes its keys from here, so
+// keys computed on different GPUs for different pages of one request compare
+// exactly as they would on one.
+__device__ __forceinline__ uint32_t group_key(const float4& v, float z0, float z1, float z2, float z3) {
+  float avg = 0.25f * (fast_exp2(v.x * kLog2e - z0) + fast_exp2(v.y * kLog2e - z1) +
+                       fast_exp2(v.z * kLog2e - z2) + fast_exp2(v.w * kLog2e - z3));
+  if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
+  return __float_as_uint(avg);
+}
+
+// log2 Z_g of unit `unit` and head g from the per-shard (max, sum) pairs of
+// the unit's pages held by `n_shards` GPUs: pairs[(shard * units + unit) * 4 + g]
+// = (max over the shard's pages of s * log2(e), sum of 2^(s log2(e) - max)).
+__device__ __forceinline__ float z_from_shards(const float2* pairs, int n_shards, int units, int unit, int g) {
+  float mx = -INFINITY, sv = 0.f;
+  for (int r = 0; r < n_shards; ++r) {
+    const float2 pr = pairs[((int64_t)r * units + unit) * kGroup + g];
+    lse2_merge(mx, sv, pr.x, pr.y);
+  }
+  return mx + fast_log2(sv);
+}
+
 // Result of cluster_select for the calling CTA.
 struct ClusterSel {
   int n;        // full pages of the request (0 when its length is invalid)
@@ -144,8 +169,11 @@ struct SelScratch {
 // Selects the pages of unit (b, h) = blockIdx.y.  Every thread of every CTA
 // of the cluster must call it.  Writes `selected` and `n_selected`; ends with
 // a cluster barrier after which rank 0's out_blk[0, kk) may be read through
-// distributed shared memory.
-template <int C, bool kStaged>
+// distributed shared memory.  kExtZ: Z_g is not formed from this unit's
+// scores but taken from p.zpairs (per-shard (max, sum) pairs of a request
+// whose pages several GPUs hold); the scores and pages are then this GPU's
+// shard of the request.
+template <int C, bool kStaged, bool kExtZ = false>
 static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScratch& sc) {
   __shared__ __align__(16) int hist0[1 << 11];
   __shared__ __align__(16) int hist1[1 << 10];
@@ -229,7 +257,11 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       pre[r] = i < len ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  {
+  if constexpr (kExtZ) {
+    if (tid < kGroup) zl[tid] = z_from_shards(reinterpret_cast<const float2*>(p.zpairs), p.z_shards,
+                                              p.batch * p.H_kv, unit, tid);
+    __syncthreads();   // zl and the cleared histograms are visible
+  } else {
     float m[kGroup] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     float s[kGroup] = {0.f, 0.f, 0.f, 0.f};
     // fold kPre scores (an absent one is -inf) into (m, s): the batch's max
@@ -286,19 +318,19 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
       lse_pub[tid][0] = mx;
       lse_pub[tid][1] = sv;
     }
-  }
-  cluster.sync();   // every CTA's (max, sum) pairs and cleared histograms are visible
-  if (tid < kGroup) {
-    float2 pr[C];   // issue every remote load before merging
+    cluster.sync();   // every CTA's (max, sum) pairs and cleared histograms are visible
+    if (tid < kGroup) {
+      float2 pr[C];   // issue every remote load before merging
 #pragma unroll
-    for (int r = 0; r < C; ++r)
-      pr[r] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(&lse_pub[tid][0], r));
-    float mx = -INFINITY, sv = 0.f;
+      for (int r = 0; r < C; ++r)
+        pr[r] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(&lse_pub[tid][0], r));
+      float mx = -INFINITY, sv = 0.f;
 #pragma unroll
-    for (int r = 0; r < C; ++r) lse2_merge(mx, sv, pr[r].x, pr[r].y);
-    zl[tid] = mx + fast_log2(sv);   // log2 Z_g
+      for (int r = 0; r < C; ++r) lse2_merge(mx, sv, pr[r].x, pr[r].y);
+      zl[tid] = mx + fast_log2(sv);   // log2 Z_g
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- 2. keys of this slice: mean over heads of exp(s - Z_g), as fp32 bits
   {
@@ -306,10 +338,7 @@ static __device__ ClusterSel cluster_select(const SelectParams& p, const SelScra
     uint32_t kmax = 0u;
     bool any = false;
     auto make_key = [&](const float4& v, int i) {
-      float avg = 0.25f * (fast_exp2(v.x * kLog2e - z0) + fast_exp2(v.y * kLog2e - z1) +
-                           fast_exp2(v.z * kLog2e - z2) + fast_exp2(v.w * kLog2e - z3));
-      if (!(avg >= 0.f) || isinf(avg)) avg = 0.f;
-      const uint32_t key = __float_as_uint(avg);
+      const uint32_t key = group_key(v, z0, z1, z2, z3);
       sc.keys_s[i] = key;
       atomicAdd(&hist0[lvl_digit(key, 0)], 1);
       kmax = max(kmax, key);

@@ -203,7 +203,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   }
 
   float* orow = p.out + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup) * kHeadDim;
+  // context-parallel shards export the unnormalised state instead
+  float* srow = p.state_out ? p.state_out + ((int64_t)b * p.H_kv * kGroup + (int64_t)h * kGroup) * kPartStride
+                            : nullptr;
   if (p.splits == 1) {
+    if (srow) {
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        srow[g * kPartStride + 2 + d] = Og[g];
+        if (d == 0) {
+          srow[g * kPartStride] = Mg[g];
+          srow[g * kPartStride + 1] = Lg[g];
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) orow[g * kHeadDim + d] = Lg[g] > 0.f ? Og[g] / Lg[g] : 0.f;
     return;
@@ -290,8 +304,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     acc_o[2] += wv.z * __ldcg(q + 2 * kPartStride);
     acc_o[3] += wv.w * __ldcg(q + 3 * kPartStride);
   }
+  if (srow) {
 #pragma unroll
-  for (int g = 0; g < kGroup; ++g) orow[g * kHeadDim + d] = Lall[g] > 0.f ? acc_o[g] / Lall[g] : 0.f;
+    for (int g = 0; g < kGroup; ++g) {
+      srow[g * kPartStride + 2 + d] = acc_o[g];
+      if (d == 0) {
+        srow[g * kPartStride] = Mall[g];
+        srow[g * kPartStride + 1] = Lall[g];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) orow[g * kHeadDim + d] = Lall[g] > 0.f ? acc_o[g] / Lall[g] : 0.f;
+  }
   if (threadIdx.x == 0) p.tickets[unit] = 0;   // ready for the next call
 }
 

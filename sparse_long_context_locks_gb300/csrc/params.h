@@ -35,6 +35,10 @@ struct SelectParams {
   uint32_t* status;
   int batch, max_pages, H_kv, budget;
   int stage_scores;        // 1: each CTA copies its slice of scores to shared memory first
+  // context-parallel selection only: Z_g from per-shard (max, sum) pairs
+  // [z_shards][batch * H_kv][G] (float2, log2 units) instead of the scores
+  const float* zpairs;
+  int z_shards;
 };
 
 struct AttnParams {
@@ -44,6 +48,7 @@ struct AttnParams {
   const int32_t* selected;     // sparse only
   const int32_t* n_selected;   // sparse only
   float* out;
+  float* state_out;            // optional: [batch][H_kv*G][2 + 128] unnormalised (m log2, l, o) instead of out
   float* part;                 // [units][splits][G][2 + 128]
   uint32_t* tickets;           // [units]
   uint32_t* status;
@@ -82,5 +87,28 @@ cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStr
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream);
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream);
+// unquantised fp32 records of rank r <= 16 (cfg quant = 0)
+cudaError_t launch_build_debug(const BuildParams& p, int rank_r, cudaStream_t stream);
+cudaError_t launch_score_debug(const ScoreParams& p, int rank_r, cudaStream_t stream);
+// shared-basis ablation (shared_basis.cu)
+cudaError_t launch_shared_basis_build(const __nv_bfloat16* k_cache, int64_t num_blocks, const int32_t* block_ids,
+                                      int n_build, int H, const float* basis, int rho, uint8_t* records,
+                                      uint32_t* status, cudaStream_t stream);
+cudaError_t launch_shared_basis_score(const __nv_bfloat16* q, const float* basis, int rho, const uint8_t* records,
+                                      int64_t num_blocks, const int32_t* block_table, const int32_t* seq_lens,
+                                      int batch, int H, int max_pages, float* scores, uint32_t* status,
+                                      cudaStream_t stream);
+
+// context-parallel shards (context_parallel.cu)
+cudaError_t launch_cp_pairs(const int32_t* shard_lens, const float* scores, float* pairs, uint32_t* status,
+                            int units, int H, int max_pages, cudaStream_t stream);
+cudaError_t launch_cp_candidates(const float* scores, const float* zpairs, int n_shards, const int32_t* page_offset,
+                                 int32_t* pages, uint32_t* keys, const int32_t* counts, int units, int H,
+                                 int max_pages, int budget, cudaStream_t stream);
+bool cp_merge_fits(int n_shards, int budget);
+cudaError_t launch_cp_merge_select(const int32_t* cand_pages, const uint32_t* cand_keys, const int32_t* cand_counts,
+                                   int n_shards, int shard, const int32_t* page_offset, int32_t* selected,
+                                   int32_t* n_selected, int units, int H, int budget, cudaStream_t stream);
+cudaError_t launch_cp_merge_attn(const float* states, int n_shards, int rows, float* out, cudaStream_t stream);
 
 }  // namespace locks

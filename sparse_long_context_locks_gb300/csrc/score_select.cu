@@ -167,10 +167,13 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
                  __fmul_rn(d2[1][1], sc_c0)};
   float x1[4] = {__fmul_rn(d2[0][2], sc_c1), __fmul_rn(d2[0][3], sc_c1), __fmul_rn(d2[1][2], sc_c1),
                  __fmul_rn(d2[1][3], sc_c1)};
-  // The sums of 2^x are taken without a max shift while both stay inside
+  // The sums of 2^x are taken without a max shift while they stay inside
   // [2^-100, 2^100], where every term above 2^-126 is a normal float and the
-  // terms flushed to zero change the sum by less than 2^-22 of itself;
-  // otherwise the warp redoes them with each row's max taken out.
+  // terms flushed to zero change the sum by less than 2^-22 of itself; a row
+  // (page, head) whose sum leaves that range is redone with its max taken
+  // out.  The choice is the row's own (all four lanes of a row quad hold the
+  // same sum), so a page's score never depends on the other pages of its
+  // group, or on stale slots past a unit's last page.
   float m0 = 0.f, m1 = 0.f;
   float e0 = 0.f, e1 = 0.f;
 #pragma unroll
@@ -182,25 +185,33 @@ __device__ __forceinline__ void score_group4(const uint8_t* rec0, const uint32_t
   e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
   e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
   e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
-  const bool in_range = e0 >= 0x1p-100f && e0 <= 0x1p100f && e1 >= 0x1p-100f && e1 <= 0x1p100f;
-  if (!__all_sync(0xffffffffu, in_range)) {
-    m0 = fmaxf(fmaxf(x0[0], x0[1]), fmaxf(x0[2], x0[3]));
-    m1 = fmaxf(fmaxf(x1[0], x1[1]), fmaxf(x1[2], x1[3]));
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-    e0 = 0.f;
-    e1 = 0.f;
+  const bool in0 = e0 >= 0x1p-100f && e0 <= 0x1p100f;
+  const bool in1 = e1 >= 0x1p-100f && e1 <= 0x1p100f;
+  if (!__all_sync(0xffffffffu, in0 && in1)) {   // shuffles below need the whole warp
+    float n0 = fmaxf(fmaxf(x0[0], x0[1]), fmaxf(x0[2], x0[3]));
+    float n1 = fmaxf(fmaxf(x1[0], x1[1]), fmaxf(x1[2], x1[3]));
+    n0 = fmaxf(n0, __shfl_xor_sync(0xffffffffu, n0, 1));
+    n1 = fmaxf(n1, __shfl_xor_sync(0xffffffffu, n1, 1));
+    n0 = fmaxf(n0, __shfl_xor_sync(0xffffffffu, n0, 2));
+    n1 = fmaxf(n1, __shfl_xor_sync(0xffffffffu, n1, 2));
+    float f0 = 0.f, f1 = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      e0 += fast_exp2(__fsub_rn(x0[i], m0));
-      e1 += fast_exp2(__fsub_rn(x1[i], m1));
+      f0 += fast_exp2(__fsub_rn(x0[i], n0));
+      f1 += fast_exp2(__fsub_rn(x1[i], n1));
     }
-    e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
-    e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
-    e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
-    e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
+    f0 += __shfl_xor_sync(0xffffffffu, f0, 1);
+    f1 += __shfl_xor_sync(0xffffffffu, f1, 1);
+    f0 += __shfl_xor_sync(0xffffffffu, f0, 2);
+    f1 += __shfl_xor_sync(0xffffffffu, f1, 2);
+    if (!in0) {
+      m0 = n0;
+      e0 = f0;
+    }
+    if (!in1) {
+      m1 = n1;
+      e1 = f1;
+    }
   }
 
   // ---- centroid term for the two rows, fetched from the mu tile's lanes
@@ -478,7 +489,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 
 // One cluster of C CTAs per (request, KV head).
 // kStaged: each CTA first copies its slice of scores to shared memory.
-template <int C, bool kStaged>
+// kExtZ: Z_g comes from per-shard (max, sum) pairs (context-parallel shards).
+template <int C, bool kStaged, bool kExtZ>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) select_kernel(const SelectParams p) {
   // launched as a programmatic dependent of the scoring pass, and the split-K
   // attention as one of this kernel
@@ -494,7 +506,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) sele
   sc.stage = kStaged ? reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(sel_dyn) +
                                                  select_stage_offset(p.max_pages, p.budget, C))
                      : nullptr;
-  cluster_select<C, kStaged>(p, sc);
+  cluster_select<C, kStaged, kExtZ>(p, sc);
 }
 
 }  // namespace locks
@@ -521,11 +533,12 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
   }
 }
 
-template <int C, bool kStaged>
+template <int C, bool kStaged, bool kExtZ = false>
 cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t stream) {
   const size_t dyn = select_smem_bytes(p.max_pages, p.budget, C, kStaged);
   static DynSmemAttr smem_attr;
-  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C, kStaged>), dyn, smem_attr);
+  const cudaError_t e =
+      ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C, kStaged, kExtZ>), dyn, smem_attr);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, units, 1);
@@ -537,13 +550,22 @@ cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t el = cudaLaunchKernelEx(&cfg, select_kernel<C, kStaged>, p);
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, select_kernel<C, kStaged, kExtZ>, p);
   if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 
 cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream) {
   const bool staged = p.stage_scores != 0;
+  if (p.zpairs != nullptr) {   // context-parallel shard: Z_g given, scores read from L2
+    switch (cluster) {
+      case 8: return launch_select_c<8, false, true>(p, units, stream);
+      case 4: return launch_select_c<4, false, true>(p, units, stream);
+      case 2: return launch_select_c<2, false, true>(p, units, stream);
+      case 1: return launch_select_c<1, false, true>(p, units, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (cluster) {
     case 8: return staged ? launch_select_c<8, true>(p, units, stream) : launch_select_c<8, false>(p, units, stream);
     case 4: return staged ? launch_select_c<4, true>(p, units, stream) : launch_select_c<4, false>(p, units, stream);

@@ -36,8 +36,15 @@ class locks_cfg(ctypes.Structure):
                 ("group_size", ctypes.c_int32), ("quant", ctypes.c_int32)]
 
 
-def make_cfg(num_kv_heads: int, group_size: int = GROUP) -> locks_cfg:
-    return locks_cfg(HEAD_DIM, PAGE_SIZE, RANK, num_kv_heads, group_size, 1)
+def make_cfg(num_kv_heads: int, group_size: int = GROUP, quant: int = 1, rank: int = RANK) -> locks_cfg:
+    """quant=1: the 784-byte int4/int8 records at rank 8; quant=0: unquantised
+    fp32 records of rank 1..16 (record_bytes(0, rank) bytes)."""
+    return locks_cfg(HEAD_DIM, PAGE_SIZE, rank, num_kv_heads, group_size, quant)
+
+
+def record_bytes(quant: int = 1, rank: int = RANK) -> int:
+    """Bytes of one page-head summary record (see include/locks.h)."""
+    return RECORD_BYTES if quant == 1 else 528 + 576 * rank
 
 
 _lib = None
@@ -69,6 +76,15 @@ _SIGS = {
                                            _I32, _F, _P, _P]),
     "locks_noalloc_read_status": (_I32, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "locks_check_bounded_wait": (_I32, [_P, _P, ctypes.c_uint32, _P, _SZ, _P]),
+    "locks_shared_basis_build": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _I32, _P, _P, _SZ, _P]),
+    "locks_shared_basis_score": (_I32, [_CFG, _P, _P, _I32, _P, _I64, _P, _P, _I32, _I32, _P, _P, _SZ, _P]),
+    "locks_cp_score_pairs": (_I32, [_CFG, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "locks_cp_select_local": (_I32, [_CFG, _P, _P, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ,
+                                     _P]),
+    "locks_cp_merge_select": (_I32, [_CFG, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "locks_cp_sparse_decode_partial": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32, _I32,
+                                              _F, _P, _P, _SZ, _P]),
+    "locks_cp_merge_attention": (_I32, [_CFG, _I32, _I32, _P, _P, _P]),
 }
 
 
@@ -114,8 +130,8 @@ def _check(status: int, where: str) -> None:
 
 
 # ------------------------------------------------------------------ sizes
-def locks_summary_bytes(num_kv_heads: int) -> int:
-    cfg = make_cfg(num_kv_heads)
+def locks_summary_bytes(num_kv_heads: int, quant: int = 1, rank: int = RANK) -> int:
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     return int(load().locks_summary_bytes(ctypes.byref(cfg)))
 
 
@@ -199,12 +215,13 @@ def _req_selection(H, B, budget_pages, selected, n_selected) -> None:
 
 
 # ------------------------------------------------------------------ calls
-def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace=None, stream=None):
+def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace=None, stream=None,
+                          quant=1, rank=RANK):
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(block_ids, "block_ids", "int32", (None,))
-    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, RECORD_BYTES))
+    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, record_bytes(quant, rank)))
     _req(workspace, "workspace", "uint8", optional=True)
-    cfg = make_cfg(num_kv_heads)
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     _check(load().locks_build_summaries(
         ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), block_ids.numel(),
         _ptr(summaries), _ptr(workspace), _nbytes(workspace), _stream(stream)),
@@ -212,16 +229,16 @@ def locks_build_summaries(num_kv_heads, k_cache, block_ids, summaries, workspace
 
 
 def locks_build_pending(num_kv_heads, k_cache, block_ids, n_pending, summaries, workspace=None,
-                        stream=None):
+                        stream=None, quant=1, rank=RANK):
     """Build the records of block_ids[0, n_pending[0]) (n_pending: a device
     int32 tensor, read by the kernel); block_ids holds room for the most pages
     any step can finalise."""
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(block_ids, "block_ids", "int32", (None,))
     _req(n_pending, "n_pending", "int32", (None,))
-    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, RECORD_BYTES))
+    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, record_bytes(quant, rank)))
     _req(workspace, "workspace", "uint8", optional=True)
-    cfg = make_cfg(num_kv_heads)
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     _check(load().locks_build_pending(
         ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), _ptr(n_pending),
         block_ids.numel(), _ptr(summaries), _ptr(workspace), _nbytes(workspace), _stream(stream)),
@@ -229,12 +246,12 @@ def locks_build_pending(num_kv_heads, k_cache, block_ids, n_pending, summaries, 
 
 
 def locks_score(num_kv_heads, q, summaries, block_table, seq_lens, workspace, scores=None,
-                stream=None):
+                stream=None, quant=1, rank=RANK):
     B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
-    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, record_bytes(quant, rank)))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req(workspace, "workspace", "uint8")
-    cfg = make_cfg(num_kv_heads)
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     _check(load().locks_score(
         ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
         _ptr(seq_lens), block_table.shape[0], block_table.shape[1], _ptr(scores), _ptr(workspace),
@@ -256,13 +273,13 @@ def locks_select(num_kv_heads, seq_lens, max_pages, budget_pages, selected, n_se
 
 
 def locks_score_select(num_kv_heads, q, summaries, block_table, seq_lens, budget_pages, selected,
-                       n_selected, workspace, scores=None, stream=None):
+                       n_selected, workspace, scores=None, stream=None, quant=1, rank=RANK):
     B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
-    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, record_bytes(quant, rank)))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
     _req(workspace, "workspace", "uint8")
-    cfg = make_cfg(num_kv_heads)
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     _check(load().locks_score_select(
         ctypes.byref(cfg), _ptr(q), _ptr(summaries), summaries.shape[0], _ptr(block_table),
         _ptr(seq_lens), block_table.shape[0], block_table.shape[1], budget_pages, _ptr(scores),
@@ -308,16 +325,16 @@ def locks_select_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, s
 
 def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table, seq_lens,
                       budget_pages, selected, n_selected, out, workspace, scores=None,
-                      sm_scale=None, stream=None):
+                      sm_scale=None, stream=None, quant=1, rank=RANK):
     B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
-    _req(summaries, "summaries", "uint8", (None, num_kv_heads, RECORD_BYTES))
+    _req(summaries, "summaries", "uint8", (None, num_kv_heads, record_bytes(quant, rank)))
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
     _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
     _req(workspace, "workspace", "uint8")
-    cfg = make_cfg(num_kv_heads)
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_decode_step(
         ctypes.byref(cfg), _ptr(q), _ptr(summaries), _ptr(k_cache), _ptr(v_cache),
@@ -378,6 +395,115 @@ def locks_check_bounded_wait(src, result, limit_us, workspace, stream=None) -> N
     _check(load().locks_check_bounded_wait(_ptr(src), _ptr(result), int(limit_us), _ptr(workspace),
                                            _nbytes(workspace), _stream(stream)),
            "locks_check_bounded_wait")
+
+
+# ------------------------------------------------------------------ shared-basis ablation
+def shared_basis_record_bytes(rho: int) -> int:
+    return 512 + 64 * rho
+
+
+def locks_shared_basis_build(num_kv_heads, k_cache, block_ids, basis, records, workspace=None, stream=None):
+    """basis: float32 [H_kv, 128, rho]; records: uint8 [num_blocks, H_kv, 512 + 64 rho]."""
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(block_ids, "block_ids", "int32", (None,))
+    _req(basis, "basis", "float32", (num_kv_heads, HEAD_DIM, None))
+    rho = basis.shape[2]
+    _req(records, "records", "uint8", (k_cache.shape[0], num_kv_heads, shared_basis_record_bytes(rho)))
+    _req(workspace, "workspace", "uint8", optional=True)
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_shared_basis_build(
+        ctypes.byref(cfg), _ptr(k_cache), k_cache.shape[0], _ptr(block_ids), block_ids.numel(), _ptr(basis), rho,
+        _ptr(records), _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_shared_basis_build")
+
+
+def locks_shared_basis_score(num_kv_heads, q, basis, records, block_table, seq_lens, workspace, scores=None,
+                             stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req(basis, "basis", "float32", (num_kv_heads, HEAD_DIM, None))
+    rho = basis.shape[2]
+    _req(records, "records", "uint8", (None, num_kv_heads, shared_basis_record_bytes(rho)))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req(workspace, "workspace", "uint8")
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_shared_basis_score(
+        ctypes.byref(cfg), _ptr(q), _ptr(basis), rho, _ptr(records), records.shape[0], _ptr(block_table),
+        _ptr(seq_lens), B, MP, _ptr(scores), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_shared_basis_score")
+
+
+# ------------------------------------------------------------------ context-parallel shards
+# One request's pages split over several GPUs; see include/locks.h.  Every
+# tensor is this shard's own; *_all tensors stack every shard's result on a
+# leading axis (gathered by the caller).
+def locks_cp_score_pairs(num_kv_heads, shard_lens, max_pages, pairs, workspace, scores=None, stream=None):
+    _req(shard_lens, "shard_lens", "int32", (None,))
+    B = shard_lens.shape[0]
+    _req(pairs, "pairs", "float32", (B, num_kv_heads, GROUP, 2))
+    _req(scores, "scores", "float32", (B, num_kv_heads, max_pages, GROUP), optional=True)
+    _req(workspace, "workspace", "uint8")
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_cp_score_pairs(ctypes.byref(cfg), _ptr(shard_lens), B, max_pages, _ptr(scores),
+                                       _ptr(pairs), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "locks_cp_score_pairs")
+
+
+def locks_cp_select_local(num_kv_heads, shard_lens, page_offset, max_pages, budget_pages, pairs_all,
+                          cand_pages, cand_keys, cand_counts, workspace, scores=None, stream=None):
+    _req(shard_lens, "shard_lens", "int32", (None,))
+    B = shard_lens.shape[0]
+    _req(page_offset, "page_offset", "int32", (B,))
+    _req(pairs_all, "pairs_all", "float32", (None, B, num_kv_heads, GROUP, 2))
+    _req(scores, "scores", "float32", (B, num_kv_heads, max_pages, GROUP), optional=True)
+    _req(cand_pages, "cand_pages", "int32", (B, num_kv_heads, max(1, budget_pages)))
+    _req(cand_keys, "cand_keys", "int32", (B, num_kv_heads, max(1, budget_pages)))
+    _req(cand_counts, "cand_counts", "int32", (B, num_kv_heads))
+    _req(workspace, "workspace", "uint8")
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_cp_select_local(
+        ctypes.byref(cfg), _ptr(shard_lens), _ptr(page_offset), B, max_pages, budget_pages, _ptr(scores),
+        _ptr(pairs_all), pairs_all.shape[0], _ptr(cand_pages), _ptr(cand_keys), _ptr(cand_counts),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_cp_select_local")
+
+
+def locks_cp_merge_select(num_kv_heads, page_offset, budget_pages, shard, cand_pages_all, cand_keys_all,
+                          cand_counts_all, selected, n_selected, stream=None):
+    _req(page_offset, "page_offset", "int32", (None,))
+    B = page_offset.shape[0]
+    R = cand_counts_all.shape[0]
+    _req(cand_pages_all, "cand_pages_all", "int32", (R, B, num_kv_heads, max(1, budget_pages)))
+    _req(cand_keys_all, "cand_keys_all", "int32", (R, B, num_kv_heads, max(1, budget_pages)))
+    _req(cand_counts_all, "cand_counts_all", "int32", (R, B, num_kv_heads))
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_cp_merge_select(
+        ctypes.byref(cfg), _ptr(page_offset), B, budget_pages, R, shard, _ptr(cand_pages_all),
+        _ptr(cand_keys_all), _ptr(cand_counts_all), _ptr(selected), _ptr(n_selected), _stream(stream)),
+        "locks_cp_merge_select")
+
+
+def locks_cp_sparse_decode_partial(num_kv_heads, q, k_cache, v_cache, block_table, shard_lens, selected,
+                                   n_selected, budget_pages, states, workspace, sm_scale=None, stream=None):
+    B, MP = _req_step(num_kv_heads, q, block_table, shard_lens)
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(states, "states", "float32", (B, num_kv_heads * GROUP, 2 + HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
+    cfg = make_cfg(num_kv_heads)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_cp_sparse_decode_partial(
+        ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_table),
+        _ptr(shard_lens), _ptr(selected), _ptr(n_selected), B, MP, budget_pages, scale, _ptr(states),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "locks_cp_sparse_decode_partial")
+
+
+def locks_cp_merge_attention(num_kv_heads, states_all, out, stream=None):
+    R, B = states_all.shape[0], states_all.shape[1]
+    _req(states_all, "states_all", "float32", (R, B, num_kv_heads * GROUP, 2 + HEAD_DIM))
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    cfg = make_cfg(num_kv_heads)
+    _check(load().locks_cp_merge_attention(ctypes.byref(cfg), B, R, _ptr(states_all), _ptr(out),
+                                           _stream(stream)), "locks_cp_merge_attention")
 
 
 def locks_status_str(status: int) -> str:

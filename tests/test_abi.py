@@ -38,6 +38,10 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizes_and_status_strings(lib):
     assert L.locks_summary_bytes(8) == 784
+    # unquantised fp32 records: mu, V (128 x r), C (16 x r), tail + pad
+    for r in (1, 8, 16):
+        assert L.locks_summary_bytes(8, quant=0, rank=r) == 4 * (128 + 128 * r + 16 * r + 4)
+        assert L.record_bytes(0, r) == L.locks_summary_bytes(8, quant=0, rank=r)
     cfg_bad = L.locks_cfg(128, 16, 8, 8, 3, 1)   # G = 3 unsupported
     assert lib.locks_summary_bytes(ctypes.byref(cfg_bad)) == 0
     small = L.locks_workspace_bytes(8, 1, 257, 16)
@@ -54,7 +58,8 @@ def test_host_validation_rejects_before_launch(lib):
     misaligned = ctypes.c_void_p(0x10001)
     # unsupported shapes
     for bad in (L.locks_cfg(64, 16, 8, 8, 4, 1), L.locks_cfg(128, 32, 8, 8, 4, 1),
-                L.locks_cfg(128, 16, 4, 8, 4, 1), L.locks_cfg(128, 16, 8, 8, 4, 0),
+                L.locks_cfg(128, 16, 4, 8, 4, 1), L.locks_cfg(128, 16, 17, 8, 4, 0),
+                L.locks_cfg(128, 16, 0, 8, 4, 0), L.locks_cfg(128, 16, 8, 8, 4, 2),
                 L.locks_cfg(128, 16, 8, 3, 4, 1), L.locks_cfg(128, 16, 8, 12, 4, 1)):
         assert lib.locks_score(ctypes.byref(bad), fake, fake, 10, fake, fake, 1, 4, None, fake,
                                1 << 20, None) == UNSUPPORTED
