@@ -537,23 +537,37 @@ def main():
     us_build = time_graph(g_build, reps=max(5, R // 10))
     n_page_heads = int(blocks.numel()) * H
     # page crossing: one page per request became full (stand-in: B distinct
-    # full blocks), built from a device-side count, alone and ahead of a step
+    # full blocks), built alone from a device-side count
     pend_ids = blocks[:B].to(torch.int32).contiguous()
     n_pend = torch.full((1,), int(pend_ids.numel()), dtype=torch.int32, device="cuda")
     g_pend = capture(lambda s: L.locks_build_pending(H, data["k_cache"], pend_ids, n_pend, summ,
                                                      bufs.workspace, stream=s))
     us_pend = time_graph(g_pend)
+    # a step whose current token completes every request's last page: the
+    # same requests one token shorter in the cache (L % 16 == 0), through
+    # locks_decode_step_crossing (the build overlapped with the scoring)
+    cross_lens = torch.where(data["seq_lens"] % 16 == 0, data["seq_lens"],
+                             data["seq_lens"] - data["seq_lens"] % 16).contiguous()
 
     def crossing_step(s):
-        L.locks_build_pending(H, data["k_cache"], pend_ids, n_pend, summ, bufs.workspace, stream=s)
-        case.step_calls(s)
+        L.locks_decode_step_crossing(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
+                                     cross_lens, w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                                     bufs.workspace, scores=bufs.scores, stream=s)
     g_cross = capture(crossing_step)
     us_cross = time_graph(g_cross)
+
+    def plain_short_step(s):   # the same shorter requests without the build
+        L.locks_decode_step(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
+                            cross_lens, w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                            bufs.workspace, scores=bufs.scores, stream=s)
+    us_cross_plain = time_graph(capture(plain_short_step))
     main_rows.update({
         "build_us": us_build, "build_page_heads": n_page_heads,
         "build_GBps": (n_page_heads * (4096 + 784)) / (us_build * 1e-6) / 1e9,
         "build_pending_us": us_pend, "build_pending_page_heads": int(pend_ids.numel()) * H,
         "step_with_page_crossing_us": us_cross,
+        "step_same_lengths_without_crossing_us": us_cross_plain,
+        "crossing_over_plain_step": us_cross / us_cross_plain,
     })
 
     # ---------------------------------------------------------------- e2e

@@ -264,6 +264,25 @@ locks_status locks_decode_step(const locks_cfg *cfg, const void *q, const void *
                                int32_t *selected, int32_t *n_selected, float *out, void *workspace,
                                size_t workspace_bytes, locks_stream_t stream);
 
+/* The decode step at a page crossing, §2 "page-local spectral decomposition"
+ * (a page is summarised when it is finalised) and "implementation" (full CUDA
+ * graph): the same results as building, for every request whose current
+ * token completed a page (L_b % 16 == 0, page L_b / 16 - 1), that page's
+ * record for every KV head into `summaries`, then locks_decode_step.  The
+ * build is launched first and the scorer as its programmatic dependent: the
+ * scorer streams every other page's record while the build runs and copies
+ * the new pages' records only after it has ended.  Requests whose length is
+ * not a multiple of 16 build nothing; the pages are derived from seq_lens and
+ * the block table on the device, so one captured graph serves any batch.
+ * Same arguments, layouts and limits as locks_decode_step (summaries is
+ * written). */
+locks_status locks_decode_step_crossing(const locks_cfg *cfg, const void *q, void *summaries,
+                                        const void *k_cache, const void *v_cache, int64_t num_blocks,
+                                        const int32_t *block_table, const int32_t *seq_lens, int32_t batch,
+                                        int32_t max_pages, int32_t budget_pages, float sm_scale, float *scores,
+                                        int32_t *selected, int32_t *n_selected, float *out, void *workspace,
+                                        size_t workspace_bytes, locks_stream_t stream);
+
 /* Dense comparator (the full-cache attention LOCKS is measured against):
  * the same computation over every cached token of each request. */
 locks_status locks_dense_decode(const locks_cfg *cfg, const void *q, const void *k_cache,

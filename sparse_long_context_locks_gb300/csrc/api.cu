@@ -356,10 +356,17 @@ locks_status locks_build_pending(const locks_cfg* cfg, const void* k_cache, int6
   return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summaries, int64_t num_blocks,
-                         const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
-                         int32_t max_pages, float* scores, void* workspace, size_t workspace_bytes,
-                         locks_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// locks_score; with defer_crossing the scorer is a programmatic dependent of
+// the crossing build just launched on the stream, and copies the page each
+// request's current token completed only after that build has ended.
+locks_status score_impl(const locks_cfg* cfg, const void* q, const void* summaries, int64_t num_blocks,
+                        const int32_t* block_table, const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                        float* scores, void* workspace, size_t workspace_bytes, locks_stream_t stream,
+                        bool defer_crossing) {
   if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
   if (batch < 0 || max_pages < 1 || num_blocks < 1) return LOCKS_ERR_INVALID_ARG;
   if (batch == 0) return LOCKS_OK;
@@ -390,8 +397,22 @@ locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summar
   p.n_chunks = pl.n_chunks;
   p.head_groups = pl.head_groups;
   p.n_items = pl.n_items;
+  // (the fp32 scorer is launched in stream order: after the whole build)
   if (cfg->quant == 0) return from_cuda(launch_score_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
-  return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream)));
+  p.defer_crossing = defer_crossing ? 1 : 0;
+  return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream), defer_crossing));
+}
+
+}  // namespace
+
+extern "C" {
+
+locks_status locks_score(const locks_cfg* cfg, const void* q, const void* summaries, int64_t num_blocks,
+                         const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                         int32_t max_pages, float* scores, void* workspace, size_t workspace_bytes,
+                         locks_stream_t stream) {
+  return score_impl(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores, workspace,
+                    workspace_bytes, stream, false);
 }
 
 }  // extern "C"
@@ -484,11 +505,15 @@ locks_status locks_select_sparse_decode(const locks_cfg* cfg, const void* q, con
   return from_cuda(launch_select_attend(tmk, tmv, p, batch * H, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* summaries, const void* k_cache,
-                               const void* v_cache, int64_t num_blocks, const int32_t* block_table,
-                               const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
-                               float sm_scale, float* scores, int32_t* selected, int32_t* n_selected, float* out,
-                               void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+locks_status decode_step_impl(const locks_cfg* cfg, const void* q, void* summaries, const void* k_cache,
+                              const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                              const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                              float sm_scale, float* scores, int32_t* selected, int32_t* n_selected, float* out,
+                              void* workspace, size_t workspace_bytes, locks_stream_t stream, bool crossing) {
   if (!cfg_supported(cfg)) return cfg == nullptr ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
   if (budget_pages < 0 || budget_pages > kFusedMaxBudget) return budget_pages < 0 ? LOCKS_ERR_INVALID_ARG : LOCKS_ERR_UNSUPPORTED;
   if (batch > 0 && (max_pages + kSelCluster - 1) / kSelCluster > kFusedMaxKeysPerCta) return LOCKS_ERR_UNSUPPORTED;
@@ -500,8 +525,30 @@ locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* 
     if (budget_pages > 0) LOCKS_CHECK_PTR(selected);
     if (!(sm_scale > 0.f)) return LOCKS_ERR_INVALID_ARG;
   }
-  locks_status st = locks_score(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores,
-                                workspace, workspace_bytes, stream);
+  if (crossing && batch > 0) {
+    // the pages the current tokens completed: built first, the scorer
+    // overlapping all of it but those pages' copies
+    LOCKS_CHECK_PTR(k_cache);
+    LOCKS_CHECK_PTR(block_table);
+    LOCKS_CHECK_PTR(seq_lens);
+    LOCKS_CHECK_PTR(summaries);
+    LOCKS_CHECK_PTR(workspace);
+    BuildParams bp{};
+    bp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+    bp.summ = static_cast<uint8_t*>(summaries);
+    bp.status = status_word(workspace);
+    bp.num_blocks = num_blocks;
+    bp.n_build = batch;
+    bp.H_kv = cfg->num_kv_heads;
+    bp.block_table = block_table;
+    bp.seq_lens = seq_lens;
+    bp.max_pages = max_pages;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = cfg->quant == 0 ? launch_build_debug(bp, cfg->rank, s) : launch_build(bp, s);
+    if (e != cudaSuccess) return LOCKS_ERR_CUDA;
+  }
+  locks_status st = score_impl(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores,
+                               workspace, workspace_bytes, stream, crossing);
   if (st != LOCKS_OK) return st;
   // One cluster per (request, KV head): when they all fit on the GPU at once
   // the fused kernel keeps the selection on chip; with more units its
@@ -520,6 +567,31 @@ locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* 
   if (st != LOCKS_OK) return st;
   return locks_sparse_decode(cfg, q, k_cache, v_cache, num_blocks, block_table, seq_lens, selected, n_selected,
                              batch, max_pages, budget_pages, sm_scale, out, workspace, workspace_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+locks_status locks_decode_step(const locks_cfg* cfg, const void* q, const void* summaries, const void* k_cache,
+                               const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                               const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                               float sm_scale, float* scores, int32_t* selected, int32_t* n_selected, float* out,
+                               void* workspace, size_t workspace_bytes, locks_stream_t stream) {
+  return decode_step_impl(cfg, q, const_cast<void*>(summaries), k_cache, v_cache, num_blocks, block_table,
+                          seq_lens, batch, max_pages, budget_pages, sm_scale, scores, selected, n_selected, out,
+                          workspace, workspace_bytes, stream, false);
+}
+
+locks_status locks_decode_step_crossing(const locks_cfg* cfg, const void* q, void* summaries, const void* k_cache,
+                                        const void* v_cache, int64_t num_blocks, const int32_t* block_table,
+                                        const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                                        int32_t budget_pages, float sm_scale, float* scores, int32_t* selected,
+                                        int32_t* n_selected, float* out, void* workspace, size_t workspace_bytes,
+                                        locks_stream_t stream) {
+  return decode_step_impl(cfg, q, summaries, k_cache, v_cache, num_blocks, block_table, seq_lens, batch,
+                          max_pages, budget_pages, sm_scale, scores, selected, n_selected, out, workspace,
+                          workspace_bytes, stream, true);
 }
 
 locks_status locks_score_select(const locks_cfg* cfg, const void* q, const void* summaries,

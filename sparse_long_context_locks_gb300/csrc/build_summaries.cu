@@ -53,34 +53,43 @@ __host__ __device__ constexpr int jacobi_partner(int i, int r) {
   return i == 15 ? r : (i == r ? 15 : (2 * r - i + 15) % 15);
 }
 
+// The rotation of a pair and its updates, explicitly rounded (x is this
+// row's or column's element, y the partner's).
+__device__ __forceinline__ float rot_lo(float c, float s, float x, float y) { return __fmaf_rn(c, x, __fmul_rn(-s, y)); }
+__device__ __forceinline__ float rot_hi(float c, float s, float x, float y) { return __fmaf_rn(c, x, __fmul_rn(s, y)); }
+
+// (c, s) of the rotation that zeroes e in [[a, e], [e, b]].  Approximate
+// division and square root: c and s are renormalised from t, so the rotation
+// stays orthogonal whatever t's rounding.
+__device__ __forceinline__ float2 jacobi_cs(float a, float bb, float e) {
+  float c = 1.f, s = 0.f;
+  if (fabsf(e) > 1e-30f && __fmul_rn(e, e) > __fmul_rn(1e-24f, fabsf(__fmul_rn(a, bb)))) {
+    // |tau| beyond 1e18 gives a rotation below 1e-18: clamped so 1 + tau^2
+    // stays finite
+    const float tau = fminf(fmaxf(__fdividef(__fsub_rn(bb, a), 2.f * e), -1e18f), 1e18f);
+    const float r2 = __fmaf_rn(tau, tau, 1.f);
+    const float t = __fdividef(copysignf(1.f, tau), __fmaf_rn(r2, rsqrtf(r2), fabsf(tau)));
+    c = rsqrtf(__fmaf_rn(t, t, 1.f));
+    s = __fmul_rn(t, c);
+  }
+  return make_float2(c, s);
+}
+
 template <int R>
 __device__ __forceinline__ void jacobi_round(float (&g)[kPage], float (&w)[kPage], int i, int hbase,
                                              HalfWarpSmem& S) {
   const int q = jacobi_partner(i, R);
   const int lo = min(i, q), hi = max(i, q);
-  const float a = S.G[lo * kPage + lo];
-  const float bb = S.G[hi * kPage + hi];
-  const float e = S.G[lo * kPage + hi];
-  float c = 1.f, s = 0.f;
-  // (approximate division and square root: c and s are renormalised from t,
-  // so the rotation stays orthogonal whatever t's rounding)
-  if (fabsf(e) > 1e-30f && e * e > 1e-24f * fabsf(a * bb)) {
-    // |tau| beyond 1e18 gives a rotation below 1e-18: clamped so 1 + tau^2
-    // stays finite
-    const float tau = fminf(fmaxf(__fdividef(bb - a, 2.f * e), -1e18f), 1e18f);
-    const float r2 = 1.f + tau * tau;
-    const float t = __fdividef(copysignf(1.f, tau), fabsf(tau) + r2 * rsqrtf(r2));
-    c = rsqrtf(1.f + t * t);
-    s = t * c;
-  }
-  S.rot[i] = make_float2(c, s);
+  const float2 cs0 = jacobi_cs(S.G[lo * kPage + lo], S.G[hi * kPage + hi], S.G[lo * kPage + hi]);
+  const float c = cs0.x, s = cs0.y;
+  S.rot[i] = cs0;
   // row update: rows lo, hi of J^T G
   float pg[kPage];
 #pragma unroll
   for (int j = 0; j < kPage; ++j) pg[j] = __shfl_sync(0xffffffffu, g[j], hbase + q);
   const bool is_lo = (i == lo);
 #pragma unroll
-  for (int j = 0; j < kPage; ++j) g[j] = is_lo ? (c * g[j] - s * pg[j]) : (s * pg[j] + c * g[j]);
+  for (int j = 0; j < kPage; ++j) g[j] = is_lo ? rot_lo(c, s, g[j], pg[j]) : rot_hi(c, s, g[j], pg[j]);
   __syncwarp();
   // column update: (J^T G) J and W J; the pairing of column j is static
   float ng[kPage], nw[kPage];
@@ -89,11 +98,11 @@ __device__ __forceinline__ void jacobi_round(float (&g)[kPage], float (&w)[kPage
     const int pj = jacobi_partner(j, R);
     const float2 cs = S.rot[j];
     if (j < pj) {
-      ng[j] = cs.x * g[j] - cs.y * g[pj];
-      nw[j] = cs.x * w[j] - cs.y * w[pj];
+      ng[j] = rot_lo(cs.x, cs.y, g[j], g[pj]);
+      nw[j] = rot_lo(cs.x, cs.y, w[j], w[pj]);
     } else {
-      ng[j] = cs.y * g[pj] + cs.x * g[j];
-      nw[j] = cs.y * w[pj] + cs.x * w[j];
+      ng[j] = rot_hi(cs.x, cs.y, g[j], g[pj]);
+      nw[j] = rot_hi(cs.x, cs.y, w[j], w[pj]);
     }
   }
 #pragma unroll
@@ -197,7 +206,20 @@ __device__ __forceinline__ bool build_target(const BuildParams& p, int i, int64_
   bool active = ph < total;
   blk = -1;
   h = 0;
-  if (active) {
+  if (active && p.block_table != nullptr) {
+    // crossing mode: the page request b's current token completed, if any
+    const int b = (int)(ph / p.H_kv);
+    const int L = p.seq_lens[b];
+    h = (int)(ph % p.H_kv);
+    if (L > 0 && L % kPage == 0 && L / kPage <= p.max_pages)
+      blk = p.block_table[(int64_t)b * p.max_pages + L / kPage - 1];
+    else
+      active = false;
+    if (active && (blk < 0 || blk >= p.num_blocks)) {
+      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+      active = false;
+    }
+  } else if (active) {
     blk = p.block_ids[ph / p.H_kv];
     h = (int)(ph % p.H_kv);
     if (blk < 0 || blk >= p.num_blocks) {
@@ -215,6 +237,8 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   HalfWarpSmem& S = reinterpret_cast<HalfWarpSmem*>(smem_b)[warp * 2 + half];
   int64_t blk;
   int h;
+  // a scorer launched as a programmatic dependent of this build may start now
+  griddep_launch_dependents();
   // Both half-warps run every step (warp-synchronous shuffles); an inactive
   // half works on a zero page and stores nothing.
   const bool active = build_target(p, i, blk, h);

@@ -169,6 +169,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, in
       : "memory");
 }
 
+// Prefetch the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -102,6 +102,24 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     prefetch_tmap(&tmv);
   }
   __syncwarp();
+  // The request's length and block-table row are inputs, not the selection's
+  // results: the row's lines this split may touch are pulled into L2 before
+  // the wait, so the block lookup after it is an L2 hit.  (A sparse split's
+  // pages are anywhere in the row; each of the unit's CTAs prefetches its
+  // share of the row's lines.)
+  {
+    const int L0 = p.seq_lens[b];
+    if (L0 > 0 && (L0 + kPage - 1) / kPage <= p.max_pages) {
+      const int npg = (L0 + kPage - 1) / kPage;
+      const int32_t* row = p.block_table + (int64_t)b * p.max_pages;
+      const int lines = (npg + 31) / 32;   // 32 entries a line
+      const int per = (lines + p.splits - 1) / p.splits;
+      const int l0 = p.dense ? (int)((int64_t)split * p.items_per_split / 32) : split * per;
+      const int l1 = p.dense ? min(lines, (int)(((int64_t)(split + 1) * p.items_per_split + 31) / 32))
+                             : min(lines, l0 + per);
+      for (int l = l0 + threadIdx.x; l < l1; l += blockDim.x) prefetch_l2(row + 32 * l);
+    }
+  }
   // launched as a programmatic dependent of the selection: its lists are
   // visible from here on
   griddep_wait();

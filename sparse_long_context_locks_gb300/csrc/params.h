@@ -25,6 +25,9 @@ struct ScoreParams {
   int n_chunks;       // chunks per (b, head group)
   int head_groups;    // H_kv / h_cta
   int n_items;        // batch * head_groups * n_chunks
+  // 1: launched as a programmatic dependent of the crossing build; the page a
+  // request's current token completed is copied only after that build ends
+  int defer_crossing;
 };
 
 struct SelectParams {
@@ -67,6 +70,11 @@ struct BuildParams {
   uint32_t* status;
   int64_t num_blocks;
   int n_build, H_kv;
+  // crossing mode (block_ids unused): request b = page-head / H_kv builds the
+  // page its current token completed, page L_b / 16 - 1, when L_b % 16 == 0
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int max_pages;
 };
 
 struct FusedParams {
@@ -78,7 +86,7 @@ struct FusedParams {
   float scale_log2;            // sm_scale * log2(e)
 };
 
-cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream, bool programmatic = false);
 cudaError_t launch_select_attend(const CUtensorMap& tmk, const CUtensorMap& tmv, const FusedParams& p,
                                  int units, cudaStream_t stream);
 size_t fused_smem_bytes(int max_pages, int budget);

@@ -333,10 +333,13 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
     int unit = first_unit, c = it_begin - first_unit * p.n_chunks;
     int it = it_begin;
     int b = 0, hg = 0, n = 0;
+    int cross_pg = -1;   // the page the request's current token completed (deferred)
+    bool waited = false;
     auto enter_unit = [&]() {
       b = unit / p.head_groups;
       hg = unit % p.head_groups;
       n = max(request_full_pages(p, b), 0);
+      cross_pg = (p.defer_crossing && n > 0 && p.seq_lens[b] % kPage == 0) ? n - 1 : -1;
     };
     // advance (it, c, unit) to the next stage that holds pages, or it_end
     auto skip_empty = [&]() {
@@ -371,6 +374,11 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
       if (is_live && (blk < 0 || blk >= p.num_blocks)) {
         flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
         is_live = false;
+      }
+      // the crossing build's page: its record exists once that grid has ended
+      if (!waited && __any_sync(0xffffffffu, is_live && c * kPps + lane == cross_pg)) {
+        griddep_wait();
+        waited = true;
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, is_live);
       if (lane == 0) {
@@ -515,20 +523,35 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) sele
 namespace locks {
 
 template <int kHcta>
-cudaError_t launch_score_t(const ScoreParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_score_t(const ScoreParams& p, int grid, cudaStream_t stream, bool programmatic) {
   static DynSmemAttr smem_attr;
   const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(score_kernel<kHcta>), kScoreSmem, smem_attr);
   if (e != cudaSuccess) return e;
-  score_kernel<kHcta><<<grid, kScoreThreads, kScoreSmem, stream>>>(p);
+  if (!programmatic) {
+    score_kernel<kHcta><<<grid, kScoreThreads, kScoreSmem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kScoreThreads, 1, 1);
+  cfg.dynamicSmemBytes = kScoreSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, score_kernel<kHcta>, p);
+  if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 
-cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream, bool programmatic) {
   switch (p.h_cta) {
-    case 8: return launch_score_t<8>(p, grid, stream);
-    case 4: return launch_score_t<4>(p, grid, stream);
-    case 2: return launch_score_t<2>(p, grid, stream);
-    case 1: return launch_score_t<1>(p, grid, stream);
+    case 8: return launch_score_t<8>(p, grid, stream, programmatic);
+    case 4: return launch_score_t<4>(p, grid, stream, programmatic);
+    case 2: return launch_score_t<2>(p, grid, stream, programmatic);
+    case 1: return launch_score_t<1>(p, grid, stream, programmatic);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,6 +71,8 @@ _SIGS = {
                                           _P, _F, _P, _P, _SZ, _P]),
     "locks_decode_step": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _F, _P, _P,
                                  _P, _P, _P, _SZ, _P]),
+    "locks_decode_step_crossing": (_I32, [_CFG, _P, _P, _P, _P, _I64, _P, _P, _I32, _I32, _I32, _F, _P, _P,
+                                          _P, _P, _P, _SZ, _P]),
     "locks_status_str": (ctypes.c_char_p, [_I32]),
     "locks_sparse_decode_noalloc": (_I32, [_CFG, _P, _P, _P, _I64, _P, _P, _P, _P, _I32, _I32,
                                            _I32, _F, _P, _P]),
@@ -342,6 +344,29 @@ def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table,
         block_table.shape[1], budget_pages, scale, _ptr(scores), _ptr(selected),
         _ptr(n_selected), _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
         "locks_decode_step")
+
+
+def locks_decode_step_crossing(num_kv_heads, q, summaries, k_cache, v_cache, block_table, seq_lens,
+                               budget_pages, selected, n_selected, out, workspace, scores=None,
+                               sm_scale=None, stream=None, quant=1, rank=RANK):
+    """locks_decode_step after building the page each request's current token
+    completed (requests with L_b % 16 == 0), overlapped with the scoring."""
+    B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
+    _req(summaries, "summaries", "uint8", (k_cache.shape[0], num_kv_heads, record_bytes(quant, rank)))
+    _req_cache(k_cache, "k_cache", num_kv_heads)
+    _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
+    _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
+    _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
+    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req(workspace, "workspace", "uint8")
+    cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
+    scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
+    _check(load().locks_decode_step_crossing(
+        ctypes.byref(cfg), _ptr(q), _ptr(summaries), _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], _ptr(block_table), _ptr(seq_lens), block_table.shape[0],
+        block_table.shape[1], budget_pages, scale, _ptr(scores), _ptr(selected),
+        _ptr(n_selected), _ptr(out), _ptr(workspace), _nbytes(workspace), _stream(stream)),
+        "locks_decode_step_crossing")
 
 
 def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens, out, workspace,

@@ -81,3 +81,91 @@ def test_decode_across_a_page_boundary(heads):
     for h in range(H):
         check_records(summ[torch.tensor([tail_blk], device="cuda").long(), h].cpu().numpy(),
                       run.pages_f64(d["k_cache"], 0, h, page))
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_decode_step_crossing_equals_build_then_step(fused):
+    """locks_decode_step_crossing builds the page each request's current token
+    completed (overlapped with the scoring of the other pages) and decodes: the
+    records, selections and outputs equal those of locks_build_pending over
+    the same pages followed by locks_decode_step, bit for bit.  A ragged batch
+    mixes requests at a crossing (L % 16 == 0) with requests mid-page; the
+    new pages' records start as garbage, so a copy taken before the build
+    ended would show."""
+    batch = 2 if fused else 40          # 40 x 8 clusters exceed the GPU: separate path
+    w = _w(batch=batch, context=16 * 300 + 3, context_hi=16 * 420, seed=17)
+    d = W.generate(w, device="cuda")
+    H = w.num_kv_heads
+    lens = d["seq_lens"].cpu()
+    cross = torch.arange(batch) % 3 != 1               # two requests in three at a crossing
+    lens = torch.where(cross, (lens // 16) * 16, lens)
+    lens = torch.where(lens % 16 == 0, lens, lens | 1)  # the others keep a tail
+    d["seq_lens"].copy_(lens.to(torch.int32))
+    full = W.full_page_blocks(d).cuda()
+    new_pages = [(b, int(lens[b]) // 16 - 1) for b in range(batch) if int(lens[b]) % 16 == 0]
+    new_blocks = torch.tensor([int(d["block_table"][b, j]) for b, j in new_pages], dtype=torch.int32,
+                              device="cuda")
+    # every other full page is built ahead; the new ones hold garbage
+    is_new = torch.zeros(d["num_blocks"], dtype=torch.bool, device="cuda")
+    is_new[new_blocks.long()] = True
+    old = full[~is_new[full.long()]]
+    summ = torch.zeros(d["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
+    L.locks_build_summaries(H, d["k_cache"], old, summ)
+    summ[new_blocks.long()] = 0xA5
+    ref_summ = summ.clone()
+    L.locks_build_pending(H, d["k_cache"], new_blocks, torch.tensor([len(new_pages)], dtype=torch.int32,
+                                                                    device="cuda"), ref_summ)
+    a = L.DecodeBuffers(H, w.batch, w.max_pages, w.budget_pages)
+    b_ = L.DecodeBuffers(H, w.batch, w.max_pages, w.budget_pages)
+    L.locks_decode_step(H, d["q"], ref_summ, d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"],
+                        w.budget_pages, a.selected, a.n_selected, a.out, a.workspace, scores=a.scores)
+    L.locks_decode_step_crossing(H, d["q"], summ, d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"],
+                                 w.budget_pages, b_.selected, b_.n_selected, b_.out, b_.workspace,
+                                 scores=b_.scores)
+    torch.cuda.synchronize()
+    assert L.locks_read_status(a.workspace) == 0 and L.locks_read_status(b_.workspace) == 0
+    assert torch.equal(summ, ref_summ)
+    assert torch.equal(b_.n_selected, a.n_selected)
+    for bb in range(batch):
+        for h in range(H):
+            k = int(a.n_selected[bb, h])
+            assert torch.equal(b_.selected[bb, h, :k], a.selected[bb, h, :k])
+            n = int(lens[bb]) // 16
+            assert torch.equal(b_.scores[bb, h, :n], a.scores[bb, h, :n])
+    assert torch.equal(b_.out, a.out)
+    # and the step itself against the oracle, on a few units
+    run = Run(w, data=d, summ=summ)
+    for bb, h in ((0, 0), (min(2, batch - 1), 5)):
+        check_unit(run, bb, h)
+
+
+def test_decode_step_crossing_in_a_graph_replays():
+    """One captured graph of the crossing step serves successive steps."""
+    w = _w(batch=2, context=16 * 100 - 1, seed=19)          # L = 1600: at a crossing
+    d = W.generate(w, device="cuda")
+    H = w.num_kv_heads
+    summ = torch.zeros(d["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
+    L.locks_build_summaries(H, d["k_cache"], W.full_page_blocks(d).cuda(), summ)
+    ref = summ.clone()
+    last = [int(d["block_table"][b, int(d["seq_lens"][b]) // 16 - 1]) for b in range(2)]
+    summ[torch.tensor(last).long()] = 0
+    bufs = L.DecodeBuffers(H, w.batch, w.max_pages, w.budget_pages)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        L.locks_decode_step_crossing(H, d["q"], summ, d["k_cache"], d["v_cache"], d["block_table"],
+                                     d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                                     bufs.workspace, scores=bufs.scores, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            L.locks_decode_step_crossing(H, d["q"], summ, d["k_cache"], d["v_cache"], d["block_table"],
+                                         d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected,
+                                         bufs.out, bufs.workspace, scores=bufs.scores, stream=s)
+    first = bufs.out.clone()
+    for _ in range(3):
+        summ[torch.tensor(last).long()] = 0
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(summ, ref)
+        assert torch.equal(bufs.out, first)
+    assert L.locks_read_status(bufs.workspace) == 0
