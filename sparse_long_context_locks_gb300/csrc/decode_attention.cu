@@ -23,11 +23,15 @@
 
 #include <cstdint>
 
+#include <cooperative_groups.h>
+
 #include "attn_tile.cuh"
 #include "common.cuh"
 #include "params.h"
 
 namespace locks {
+
+namespace cg = cooperative_groups;
 
 
 constexpr int kAttnWarps = 4;
@@ -81,6 +85,11 @@ __device__ __forceinline__ void item_block(const AttnParams& p, int b, int h, in
   }
 }
 
+// kClusterMerge: the unit's p.splits CTAs (at most 8) form a thread-block
+// cluster and merge their states through distributed shared memory, with no
+// partials in the workspace, fence or ticket; otherwise the last CTA of the
+// unit to finish merges the partials it finds in the workspace.
+template <bool kClusterMerge>
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                 const AttnParams p) {
@@ -241,6 +250,63 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     return;
   }
 
+  if constexpr (kClusterMerge) {
+    // publish this CTA's state; CTA r then finishes dims r, r + S, r + 2S, ...
+    cg::cluster_group cluster = cg::this_cluster();
+    float* pub = reinterpret_cast<float*>(smem + 12288);   // [G][2 + 128], past the warp states
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      pub[g * kPartStride + 2 + d] = Og[g];
+      if (d == 0) {
+        pub[g * kPartStride] = Mg[g];
+        pub[g * kPartStride + 1] = Lg[g];
+      }
+    }
+    cluster.sync();   // every split's state is published
+    const int S = p.splits;
+    const int per = (kHeadDim + S - 1) / S;
+    for (int idx = threadIdx.x; idx < kGroup * per; idx += blockDim.x) {
+      const int g = idx / per, dd = split + S * (idx % per);
+      if (dd < kHeadDim) {
+        float mr[8], lr[8], orr[8], M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {   // every remote load first
+          if (r < S) {
+            const float* rp = cluster.map_shared_rank(&pub[g * kPartStride], r);
+            mr[r] = rp[0];
+            lr[r] = rp[1];
+            orr[r] = rp[2 + dd];
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < S) M = fmaxf(M, mr[r]);
+        float Ls = 0.f, Os = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r < S) {
+              const float f = fast_exp2(mr[r] - M);
+              Ls += lr[r] * f;
+              Os += orr[r] * f;
+            }
+          }
+        }
+        if (srow) {
+          srow[g * kPartStride + 2 + dd] = Os;
+          if (dd == split) {
+            srow[g * kPartStride] = M;
+            srow[g * kPartStride + 1] = Ls;
+          }
+        } else {
+          orow[g * kHeadDim + dd] = Ls > 0.f ? Os / Ls : 0.f;
+        }
+      }
+    }
+    cluster.sync();   // keep shared memory alive until every CTA has read it
+    return;
+  }
+
   float* mypart = p.part + ((int64_t)unit * p.splits + split) * kGroup * kPartStride;
 #pragma unroll
   for (int g = 0; g < kGroup; ++g) {
@@ -338,24 +404,37 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (threadIdx.x == 0) p.tickets[unit] = 0;   // ready for the next call
 }
 
-cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
-                        cudaStream_t stream) {
+template <bool kClusterMerge>
+cudaError_t launch_attn_t(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
+                          cudaStream_t stream) {
   static DynSmemAttr smem_attr;
-  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(attn_kernel), kAttnSmem, smem_attr);
+  const cudaError_t e =
+      ensure_dyn_smem(reinterpret_cast<const void*>(attn_kernel<kClusterMerge>), kAttnSmem, smem_attr);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.batch * p.H_kv, 1);
   cfg.blockDim = dim3(kAttnThreads, 1, 1);
   cfg.dynamicSmemBytes = kAttnSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kClusterMerge ? p.splits : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t el = cudaLaunchKernelEx(&cfg, attn_kernel, tmk, tmv, p);
+  cfg.numAttrs = kClusterMerge ? 2 : 1;
+  const cudaError_t el = cudaLaunchKernelEx(&cfg, attn_kernel<kClusterMerge>, tmk, tmv, p);
   if (el != cudaSuccess) return el;
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
+                        cudaStream_t stream) {
+  // 2..8 splits a unit: a cluster per unit (portable size)
+  if (p.splits >= 2 && p.splits <= 8) return launch_attn_t<true>(tmk, tmv, p, stream);
+  return launch_attn_t<false>(tmk, tmv, p, stream);
 }
 
 }  // namespace locks

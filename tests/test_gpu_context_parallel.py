@@ -36,8 +36,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _setup(seed=21):
-    w = W.Workload("cp_gpu", batch=3, context=16 * 2000 + 5, context_hi=16 * 2600 + 11, num_kv_heads=8,
+def _setup(seed=21, batch=3):
+    w = W.Workload("cp_gpu", batch=batch, context=16 * 2000 + 5, context_hi=16 * 2600 + 11, num_kv_heads=8,
                    group=4, budget_tokens=16 * 64, carriers_per_head=4, seed=seed)
     d = W.generate(w, device="cuda", tail_fill="nan")
     d["seq_lens"][2] = 16 * 40 + 7          # a short request: every full page fits the budget
@@ -92,9 +92,12 @@ def _check(w, d, one, selected, out, shard_scores=None):
     assert agree >= w.batch * H - 2, f"only {agree} units select exactly as on one GPU"
 
 
-@pytest.mark.parametrize("R", [2, 3])
-def test_cuda_shards_match_one_gpu_step(R):
-    w, d, summ, one = _setup()
+@pytest.mark.parametrize("R,batch", [(2, 3), (3, 3), (2, 6)])
+def test_cuda_shards_match_one_gpu_step(R, batch):
+    """batch 3: 24 units, 12 attention splits a unit (merged through the
+    workspace); batch 6: 48 units, 6 splits (merged in a thread-block
+    cluster)."""
+    w, d, summ, one = _setup(batch=batch)
     shards = _cuda_shards(w, d, summ, R)
     outs = run_shards(CP.decode_step, shards)
     torch.cuda.synchronize()
