@@ -25,7 +25,8 @@ Besides the contract's keys the line carries:
   rows              per-kernel event times, the dense comparator, the summary
                     builder and the page-crossing step;
   workloads         the step and per-kernel rows of the other workloads
-                    (default: one request at 1M tokens and batch 16 x 24-32K),
+                    (default: one request at 1M tokens, batch 16 x 24-32K and
+                    batch 64 x 256K),
                     measured in the same run.
 """
 
@@ -89,7 +90,7 @@ def parse():
     ap.add_argument("--workload", default="llama8b_128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--extra-workloads", default="ctx1m,batch16_32k",
+    ap.add_argument("--extra-workloads", default="ctx1m,batch16_32k,batch64_256k_lowrank",
                     help="other named workloads whose step and per-kernel rows are measured in the "
                          "same run (comma-separated; empty for none)")
     ap.add_argument("--profile-run", action="store_true",
