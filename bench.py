@@ -24,6 +24,9 @@ Besides the contract's keys the line carries:
   roofline_step     the whole step's algorithmic bytes / the step time;
   rows              per-kernel event times, the dense comparator, the summary
                     builder and the page-crossing step;
+  layers32          the step inside a 32-layer decode pass: 32 distinct copies
+                    of the layer's K/V and records, 32 steps back to back in
+                    one graph, no flush (1.9 GB of inputs a pass);
   workloads         the step and per-kernel rows of the other workloads
                     (default: one request at 1M tokens, batch 16 x 24-32K and
                     batch 64 x 256K),
@@ -93,6 +96,8 @@ def parse():
     ap.add_argument("--extra-workloads", default="ctx1m,batch16_32k,batch64_256k_lowrank",
                     help="other named workloads whose step and per-kernel rows are measured in the "
                          "same run (comma-separated; empty for none)")
+    ap.add_argument("--no-layers32", dest="layers32", action="store_false",
+                    help="skip the 32-layer pass row")
     ap.add_argument("--profile-run", action="store_true",
                     help="warm-up and timed steps only (no per-kernel rows, e2e or CPU baseline): "
                          "the command the ncu captures run")
@@ -248,6 +253,12 @@ def make_pool():
     os.environ.setdefault("MKL_NUM_THREADS", "1")
     ctx = mp.get_context("spawn")
     return ctx.Pool(cores), cores
+
+
+def by_step(w, data):
+    """Algorithmic bytes of one step of workload w (see workload.algorithmic_bytes)."""
+    from sparse_long_context_locks_gb300 import workload as W
+    return W.algorithmic_bytes(data["seq_lens"].cpu().tolist(), w.num_kv_heads, w.group, w.budget_pages)["step"]
 
 
 # ------------------------------------------------------------------ one workload's graphs
@@ -571,6 +582,46 @@ def main():
         "crossing_over_plain_step": us_cross / us_cross_plain,
     })
 
+    # ---------------------------------------------------------------- a 32-layer pass
+    # The step inside a decode pass over 32 layers: each layer has its own
+    # copy of the K/V cache and the records (the content repeats, the memory
+    # does not), the block table and lengths are shared as in a paged engine,
+    # and the 32 steps run back to back in one graph with no flush: the
+    # layers' 32 x 60 MB of inputs are far larger than L2, so every layer's
+    # data comes from HBM while the kernels' code stays cached, as in real
+    # decoding.
+    n_layers = 32
+    layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
+    layers32 = None
+    if args.layers32 and torch.cuda.mem_get_info()[0] > n_layers * layer_bytes + (8 << 30):
+        kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_layers)]
+
+        def pass32(s):
+            for kc, vc, sm in kv:
+                L.locks_decode_step(H, data["q"], sm, kc, vc, data["block_table"], data["seq_lens"],
+                                    w.budget_pages, bufs.selected, bufs.n_selected, bufs.out, bufs.workspace,
+                                    scores=bufs.scores, stream=s)
+        g32 = capture(pass32)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g32.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 20
+            e0.record(stream)
+            for _ in range(reps):
+                g32.replay()
+            e1.record(stream)
+        e1.synchronize()
+        us32 = e0.elapsed_time(e1) * 1e3 / (reps * n_layers)
+        layers32 = {"us_per_layer": us32, "tokens_per_s_per_layer": B / (us32 * 1e-6),
+                    "layers": n_layers, "bytes_per_pass": n_layers * by_step(w, data),
+                    "GBps": by_step(w, data) / (us32 * 1e-6) / 1e9,
+                    "mode": "32 locks_decode_step calls over 32 distinct copies of the layer's K/V and records "
+                            "in one graph, replayed back to back with no L2 flush (1.9 GB of inputs a pass)"}
+        layers32["frac"] = layers32["GBps"] / peak
+        del kv, g32
+        torch.cuda.empty_cache()
+
     # ---------------------------------------------------------------- e2e
     # the step's per-token inputs (q and the sequence lengths) packed in one
     # pinned host buffer, copied in with one copy; the step reads views of the
@@ -673,6 +724,7 @@ def main():
         "roofline_kernels": kernels,
         "roofline_step": main_rows["roofline_step"],
         "rows": main_rows,
+        "layers32": layers32,
         "workloads": others,
         "cpu_baseline": cpu,
         "status_flags": status,
