@@ -129,15 +129,30 @@ int num_sms() {
   return cached[dev];
 }
 
-// CTAs per (request, KV head) in the selection kernel (8, 4 or 2).  Its
+// CTAs per (request, KV head) in the selection kernel (16, 8, 4 or 2).  Its
 // clusters are latency-bound.  When every 8-CTA cluster of the batch is
 // resident at once (4 CTAs an SM), 8 keeps each CTA's slice shortest: one
-// request at 128K selects in ~15 us (26.6 with 2).  With more units the
+// request at 128K selects in ~15 us (26.6 with 2).  Past 2,048 pages a CTA
+// (a request of more than 256K tokens), 16-CTA clusters (non-portable, 2 CTAs
+// an SM by registers) halve the slices again when the occupancy query says
+// they are all resident at once.  With more units the
 // waves cost more than the slices save, and the smallest cluster whose slices
 // fit the per-CTA key limit is best: batch 16 x 32K selects in 14.5 us with 2
 // (16.4 with 4, 24.7 with 8), batch 64 x 256K in 85.6 us (116.5 with 8).
+bool select_stage(int units, int cluster, int max_pages, int budget);
+
 int select_cluster(int units, int max_pages, int budget) {
-  if ((int64_t)units * kSelCluster <= 4 * (int64_t)num_sms()) return kSelCluster;
+  if ((int64_t)units * kSelCluster <= 4 * (int64_t)num_sms()) {
+    // A few requests at long context: 16 CTAs a unit halve every CTA's
+    // slice, when all the clusters are resident at once.
+    if ((max_pages + kSelCluster - 1) / kSelCluster > 2048 && (int64_t)units * 16 <= 2 * (int64_t)num_sms()) {
+      const bool staged = select_stage(units, 16, max_pages, budget);
+      if (select_smem_bytes(max_pages, budget, 16, staged) <= (size_t)kSmemLimit &&
+          select16_max_clusters(select_smem_bytes(max_pages, budget, 16, staged), staged) >= units)
+        return 16;
+    }
+    return kSelCluster;
+  }
   int c = 2;
   while (c < kSelCluster && ((max_pages + c - 1) / c > kFusedMaxKeysPerCta ||
                              select_smem_bytes(max_pages, budget, c) > (size_t)kSmemLimit))
@@ -159,7 +174,8 @@ bool select_stage(int units, int cluster, int max_pages, int budget) {
   if ((max_pages + cluster - 1) / cluster <= 1024) return false;
   const size_t dyn = select_smem_bytes(max_pages, budget, cluster, true);
   if (dyn > (size_t)kSmemLimit) return false;
-  const int64_t per_sm = std::min<int64_t>(4, (int64_t)(228 * 1024) / (int64_t)(dyn + 21 * 1024));
+  const int64_t per_sm =
+      std::min<int64_t>(cluster > 8 ? 2 : 4, (int64_t)(228 * 1024) / (int64_t)(dyn + 21 * 1024));
   return (int64_t)units * cluster <= per_sm * num_sms();
 }
 

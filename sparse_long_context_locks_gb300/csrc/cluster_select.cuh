@@ -9,7 +9,7 @@
 // query heads into one table; the k largest entries (lower page index on
 // ties) are attended.
 //
-// One cluster of C CTAs per (request, KV head) (C a power of two, at most 8);
+// One cluster of C CTAs per (request, KV head) (C a power of two, at most 16);
 // CTA r owns pages [n r / C, n (r + 1) / C).
 //   1. Z_g: each CTA folds its slice's scores into a (max, sum) pair per head
 //      and publishes it in shared memory; after a cluster barrier every CTA

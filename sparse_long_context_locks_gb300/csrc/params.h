@@ -90,8 +90,9 @@ cudaError_t launch_score(const ScoreParams& p, int grid, cudaStream_t stream, bo
 cudaError_t launch_select_attend(const CUtensorMap& tmk, const CUtensorMap& tmv, const FusedParams& p,
                                  int units, cudaStream_t stream);
 size_t fused_smem_bytes(int max_pages, int budget);
-// cluster: CTAs per (request, KV head): 1, 2, 4 or 8
+// cluster: CTAs per (request, KV head): 1, 2, 4, 8 or 16
 cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream);
+int select16_max_clusters(size_t dyn, bool staged);
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream);
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream);

@@ -26,6 +26,7 @@
 // memory; the selection reads them back to form Z_{b,h,g} and rank the pages.
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "params.h"
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) score_kernel(const ScorePara
 // kStaged: each CTA first copies its slice of scores to shared memory.
 // kExtZ: Z_g comes from per-shard (max, sum) pairs (context-parallel shards).
 template <int C, bool kStaged, bool kExtZ>
-__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, 4) select_kernel(const SelectParams p) {
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kSelThreads, C > 8 ? 2 : 4) select_kernel(const SelectParams p) {
   // launched as a programmatic dependent of the scoring pass, and the split-K
   // attention as one of this kernel
   griddep_launch_dependents();
@@ -563,6 +564,11 @@ cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t strea
   const cudaError_t e =
       ensure_dyn_smem(reinterpret_cast<const void*>(select_kernel<C, kStaged, kExtZ>), dyn, smem_attr);
   if (e != cudaSuccess) return e;
+  if (C > 8) {   // a non-portable cluster size
+    const cudaError_t en = cudaFuncSetAttribute(reinterpret_cast<const void*>(select_kernel<C, kStaged, kExtZ>),
+                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (en != cudaSuccess) return en;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, units, 1);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
@@ -578,10 +584,48 @@ cudaError_t launch_select_c(const SelectParams& p, int units, cudaStream_t strea
   return cudaGetLastError();
 }
 
+// How many 16-CTA clusters of the selection kernel can be resident at once
+// with this dynamic shared memory (0 when the size is refused); cached per
+// device and size.
+int select16_max_clusters(size_t dyn, bool staged) {
+  struct Entry {
+    int dev;
+    size_t dyn;
+    bool staged;
+    int n;
+  };
+  static Entry cache[16];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].dyn == dyn && cache[i].staged == staged) return cache[i].n;
+  const void* fn = staged ? reinterpret_cast<const void*>(select_kernel<16, true, false>)
+                          : reinterpret_cast<const void*>(select_kernel<16, false, false>);
+  int n = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = dyn;
+    int clusters = 0;
+    const cudaError_t e = staged ? cudaOccupancyMaxActiveClusters(&clusters, select_kernel<16, true, false>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&clusters, select_kernel<16, false, false>, &cfg);
+    if (e == cudaSuccess) n = clusters;
+  }
+  cudaGetLastError();   // a refused query leaves no sticky error
+  if (used < 16) cache[used++] = Entry{dev, dyn, staged, n};
+  return n;
+}
+
 cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStream_t stream) {
   const bool staged = p.stage_scores != 0;
   if (p.zpairs != nullptr) {   // context-parallel shard: Z_g given, scores read from L2
     switch (cluster) {
+      case 16: return launch_select_c<16, false, true>(p, units, stream);
       case 8: return launch_select_c<8, false, true>(p, units, stream);
       case 4: return launch_select_c<4, false, true>(p, units, stream);
       case 2: return launch_select_c<2, false, true>(p, units, stream);
@@ -590,6 +634,7 @@ cudaError_t launch_select(const SelectParams& p, int units, int cluster, cudaStr
     }
   }
   switch (cluster) {
+    case 16: return staged ? launch_select_c<16, true>(p, units, stream) : launch_select_c<16, false>(p, units, stream);
     case 8: return staged ? launch_select_c<8, true>(p, units, stream) : launch_select_c<8, false>(p, units, stream);
     case 4: return staged ? launch_select_c<4, true>(p, units, stream) : launch_select_c<4, false>(p, units, stream);
     case 2: return staged ? launch_select_c<2, true>(p, units, stream) : launch_select_c<2, false>(p, units, stream);
