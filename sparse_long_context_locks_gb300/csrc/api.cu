@@ -369,7 +369,7 @@ locks_status locks_build_pending(const locks_cfg* cfg, const void* k_cache, int6
   p.n_build = max_pending;
   p.H_kv = cfg->num_kv_heads;
   if (cfg->quant == 0) return from_cuda(launch_build_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
-  return from_cuda(launch_build(p, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_build_pages(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -560,7 +560,7 @@ locks_status decode_step_impl(const locks_cfg* cfg, const void* q, void* summari
     bp.seq_lens = seq_lens;
     bp.max_pages = max_pages;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = cfg->quant == 0 ? launch_build_debug(bp, cfg->rank, s) : launch_build(bp, s);
+    const cudaError_t e = cfg->quant == 0 ? launch_build_debug(bp, cfg->rank, s) : launch_build_pages(bp, s);
     if (e != cudaSuccess) return LOCKS_ERR_CUDA;
   }
   locks_status st = score_impl(cfg, q, summaries, num_blocks, block_table, seq_lens, batch, max_pages, scores,

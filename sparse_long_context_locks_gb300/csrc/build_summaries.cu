@@ -59,17 +59,20 @@ __device__ __forceinline__ float rot_lo(float c, float s, float x, float y) { re
 __device__ __forceinline__ float rot_hi(float c, float s, float x, float y) { return __fmaf_rn(c, x, __fmul_rn(s, y)); }
 
 // (c, s) of the rotation that zeroes e in [[a, e], [e, b]].  Approximate
-// division and square root: c and s are renormalised from t, so the rotation
-// stays orthogonal whatever t's rounding.
+// reciprocal and square root (single instructions: this is the serial part of
+// every round): c and s are renormalised from t, so the rotation stays
+// orthogonal whatever t's rounding.  Every operand of those instructions is a
+// normal float (|2e| > 2e-30; 1 + tau^2, 1 + t^2 and |tau| + sqrt(1 + tau^2)
+// are at least 1).
 __device__ __forceinline__ float2 jacobi_cs(float a, float bb, float e) {
   float c = 1.f, s = 0.f;
   if (fabsf(e) > 1e-30f && __fmul_rn(e, e) > __fmul_rn(1e-24f, fabsf(__fmul_rn(a, bb)))) {
     // |tau| beyond 1e18 gives a rotation below 1e-18: clamped so 1 + tau^2
     // stays finite
-    const float tau = fminf(fmaxf(__fdividef(__fsub_rn(bb, a), 2.f * e), -1e18f), 1e18f);
+    const float tau = fminf(fmaxf(__fmul_rn(__fsub_rn(bb, a), fast_rcp(2.f * e)), -1e18f), 1e18f);
     const float r2 = __fmaf_rn(tau, tau, 1.f);
-    const float t = __fdividef(copysignf(1.f, tau), __fmaf_rn(r2, rsqrtf(r2), fabsf(tau)));
-    c = rsqrtf(__fmaf_rn(t, t, 1.f));
+    const float t = copysignf(fast_rcp(__fmaf_rn(r2, fast_rsqrt(r2), fabsf(tau))), tau);
+    c = fast_rsqrt(__fmaf_rn(t, t, 1.f));
     s = __fmul_rn(t, c);
   }
   return make_float2(c, s);
@@ -196,11 +199,10 @@ __device__ __forceinline__ void build_eigen(const BuildParams& p, HalfWarpSmem& 
   for (int sweep = 0; sweep < kSweeps; ++sweep) Sweep<0>::run(g, w, i, hbase, S);
 }
 
-// The half-warp's page-head of this launch: its block and KV head, and
-// whether it is built (a block id outside the cache is flagged and skipped).
-__device__ __forceinline__ bool build_target(const BuildParams& p, int i, int64_t& blk, int& h) {
-  const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1;
-  const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;   // page-head index
+// Page-head ph of this launch: its block and KV head, and whether it is
+// built (a block id outside the cache is flagged, by the thread that
+// reports, and skipped).
+__device__ __forceinline__ bool target_of(const BuildParams& p, int64_t ph, bool report, int64_t& blk, int& h) {
   const int n_pages = p.n_dev != nullptr ? min(p.n_build, max(0, *p.n_dev)) : p.n_build;
   const int64_t total = (int64_t)n_pages * p.H_kv;
   bool active = ph < total;
@@ -216,18 +218,42 @@ __device__ __forceinline__ bool build_target(const BuildParams& p, int i, int64_
     else
       active = false;
     if (active && (blk < 0 || blk >= p.num_blocks)) {
-      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+      if (report) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
       active = false;
     }
   } else if (active) {
     blk = p.block_ids[ph / p.H_kv];
     h = (int)(ph % p.H_kv);
     if (blk < 0 || blk >= p.num_blocks) {
-      if (i == 0) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
+      if (report) flag_status(p.status, LOCKS_FLAG_BAD_BLOCK);
       active = false;
     }
   }
   return active;
+}
+
+// The half-warp's page-head (lane i of the half).
+__device__ __forceinline__ bool build_target(const BuildParams& p, int i, int64_t& blk, int& h) {
+  const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1;
+  const int64_t ph = ((int64_t)blockIdx.x * kBuildWarps + warp) * 2 + half;
+  return target_of(p, ph, i == 0, blk, h);
+}
+
+// Byte positions in the 784-byte record (include/locks.h): the centroid code
+// of dim, the coefficient code (token, direction k), and the dim held by
+// nibble pos of basis word wi (word wi at byte 4 wi).
+__device__ __forceinline__ int rec_mu_byte(int dim) {
+  const int s = dim >> 4, wd = dim & 15, hh = wd >> 3, t = (wd & 7) >> 1, ee = wd & 1;
+  return 512 + t * 32 + s * 4 + hh * 2 + ee;
+}
+__device__ __forceinline__ int rec_coef_byte(int token, int k) {
+  const int nt = token >> 3, gd = token & 7, tk = k >> 1, ek = k & 1;
+  return 640 + (gd * 4 + tk) * 4 + nt * 2 + ek;
+}
+__device__ __forceinline__ int basis_word_dim(int wi, int pos) {
+  const int t = (wi >> 2) & 3, pp = wi & 3;
+  const int e = pos >> 2, sp = (pos & 3) >> 1, hh = pos & 1;
+  return 16 * (2 * pp + sp) + 8 * hh + 2 * t + e;
 }
 
 __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams p) {
@@ -352,19 +378,16 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // centroid codes straight into the record
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const int dim = 8 * i + e;
     int c = __float2int_rn(mu8[e] * iM);
     c = max(-127, min(127, c));
-    const int s = dim >> 4, wd = dim & 15, hh = wd >> 3, t = (wd & 7) >> 1, ee = wd & 1;
-    S.rec[512 + t * 32 + s * 4 + hh * 2 + ee] = (uint8_t)(int8_t)c;
+    S.rec[rec_mu_byte(8 * i + e)] = (uint8_t)(int8_t)c;
   }
   // coefficient codes of token i
 #pragma unroll
   for (int k = 0; k < kRank; ++k) {
     int c = __float2int_rn(crow[k] * iC);
     c = max(-127, min(127, c));
-    const int nt = i >> 3, gd = i & 7, tk = k >> 1, ek = k & 1;
-    S.rec[640 + (gd * 4 + tk) * 4 + nt * 2 + ek] = (uint8_t)(int8_t)c;
+    S.rec[rec_coef_byte(i, k)] = (uint8_t)(int8_t)c;
   }
   if (i == 0) {
     float* scl = reinterpret_cast<float*>(&S.rec[768]);
@@ -377,16 +400,12 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
   // pack basis words: lane i builds words i, i+16, ..., i+112 (word = k*16 + t*4 + p)
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
-    const int wi = i + 16 * m;
-    const int k = wi >> 4, t = (wi >> 2) & 3, pp = wi & 3;
+    const int wi = i + 16 * m, k = wi >> 4;
     uint32_t word = 0;
 #pragma unroll
-    for (int pos = 0; pos < 8; ++pos) {
-      const int e = pos >> 2, sp = (pos & 3) >> 1, hh = pos & 1;
-      const int dim = 16 * (2 * pp + sp) + 8 * hh + 2 * t + e;
-      word |= ((uint32_t)S.vcode[k * kHeadDim + dim] & 0xFu) << (4 * pos);
-    }
-    *reinterpret_cast<uint32_t*>(&S.rec[k * 64 + t * 16 + pp * 4]) = word;
+    for (int pos = 0; pos < 8; ++pos)
+      word |= ((uint32_t)S.vcode[k * kHeadDim + basis_word_dim(wi, pos)] & 0xFu) << (4 * pos);
+    *reinterpret_cast<uint32_t*>(&S.rec[4 * wi]) = word;
   }
   __syncwarp();
   if (active) {
@@ -394,6 +413,383 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
     const uint4* srcr = reinterpret_cast<const uint4*>(S.rec);
     for (int c = i; c < kRecord / 16; c += 16) dst[c] = srcr[c];
   }
+}
+
+// ---------------------------------------------------------------- a few pages
+// The pages a decode step completes are few (one a request), so their build
+// is bound by the latency of one page-head's Jacobi chain, not by
+// throughput.  build_page_kernel gives each page-head a CTA of 8 warps.  In a
+// round the 8 pairs split G into 64 2x2 blocks (r, rp) x (c, cp): warps 1 and
+// 2 each own 32 of them and apply the round's rotations (rows, then
+// columns); warps 3, 5, 6 and 7 rotate W's column pairs, one (row, pair) a
+// thread; warp 0's lanes, alone on their SM sub-partition (warps w and w + 4
+// share one; warp 4 only keeps the barriers), form the three entries of the
+// next round's pivots from the same G and rotations and take the next
+// round's (c, s), so they are ready at the one barrier a round.  Blocks keep
+// the shared-memory traffic of a round low: the pivots' loads are on the
+// critical path and share the load pipe with the blocks'.  Every step
+// (centroid, Gram, rotations, ranking, lift, quantisation) uses the same
+// operations in the same order as the half-warp build: the records are bit
+// for bit those of build_kernel.
+constexpr int kPbWarps = 8;
+constexpr int kPbThreads = kPbWarps * 32;
+constexpr int kPbRounds = kSweeps * 15;
+
+struct PageSmem {
+  float X[kPage * kXStride];           // keys, then centred keys
+  float G[2][kPage * kPage];           // current / next
+  float W[2][kPage * kPage];
+  float2 cs[2][kPage];                 // (c, signed s) of the pair holding index j, this / next round
+  float mu[kHeadDim];
+  float lift[kPage * kRank];
+  float coef[kPage * kRank];
+  int order[kPage];
+  // round R's pairs: lo | hi << 8 in pair k (ascending lo)
+  uint16_t pairs[15][8];
+  // rotation lane j, round R: the 12 word offsets of the next round's pivot
+  // entries' operands ((lo,lo), (plo,lo), (lo,plo), (plo,plo); the same for
+  // (hi,hi); (lo,hi), (plo,hi), (lo,phi), (plo,phi)) and the pair (lo, hi)
+  uint4 sched_p[15][kPage];
+  float red[3][kPbWarps];
+  float tail;
+  int8_t vcode[kRank * kHeadDim];
+  __align__(16) uint8_t rec[kRecord];
+};
+
+// A rotation with the sign of s already chosen for the index it updates:
+// -s for the lower index of its pair (rot_lo), s for the higher (rot_hi).
+__device__ __forceinline__ float rot_signed(float c, float s_signed, float x, float y) {
+  return __fmaf_rn(c, x, __fmul_rn(s_signed, y));
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+  return (uint32_t)a | (uint32_t)b << 8 | (uint32_t)c << 16 | (uint32_t)d << 24;
+}
+
+__global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParams p) {
+  __shared__ PageSmem S;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Jacobi roles
+  const bool rot = warp == 0;                                      // lanes j and j + 16 agree; j stores
+  const int j = lane & 15;
+  const bool gblk = warp == 1 || warp == 2;
+  const bool wblk = warp == 3 || warp >= 5;
+  const int gb = (warp - 1) * 32 + lane;                          // G block: row pair gb / 8, column pair gb % 8
+  const int wb = (warp == 3 ? 0 : warp - 4) * 32 + lane;          // W: row wb / 8, column pair wb % 8
+  griddep_launch_dependents();
+  int64_t blk;
+  int h;
+  if (!target_of(p, blockIdx.x, tid == 0, blk, h)) return;   // uniform over the CTA
+
+  // ---- 1. keys (key row t / 16, dims 8 (t % 16) ..), the round schedule
+  // tabled while they arrive, centroid, centred keys
+  const int kr = tid >> 4, kc = tid & 15;
+  const uint4 raw = *reinterpret_cast<const uint4*>(p.k_cache + (blk * p.H_kv + h) * (int64_t)(kPage * kHeadDim) +
+                                                    kr * kHeadDim + 8 * kc);
+  if (tid < 15 * 8) {
+    const int R = tid >> 3, k = tid & 7;
+    int seen = 0, lo = 0;
+    for (int i = 0; i < kPage; ++i) {
+      const bool first = i < jacobi_partner(i, R);
+      if (first && seen == k) lo = i;
+      seen += first;
+    }
+    S.pairs[R][k] = (uint16_t)(lo | jacobi_partner(lo, R) << 8);
+  } else if (tid >= 128) {
+    for (int x = tid - 128; x < 15 * kPage; x += kPbThreads - 128) {
+      const int R = x >> 4, jx = x & 15;
+      const int q = jacobi_partner(jx, R == 14 ? 0 : R + 1);
+      const int lo = min(jx, q), hi = max(jx, q);
+      const int plo = jacobi_partner(lo, R), phi = jacobi_partner(hi, R);
+      S.sched_p[R][jx] = make_uint4(pack4(lo * 16 + lo, plo * 16 + lo, lo * 16 + plo, plo * 16 + plo),
+                                   pack4(hi * 16 + hi, phi * 16 + hi, hi * 16 + phi, phi * 16 + phi),
+                                   pack4(lo * 16 + hi, plo * 16 + hi, lo * 16 + phi, plo * 16 + phi),
+                                   (uint32_t)lo | (uint32_t)hi << 8);
+    }
+  }
+  {
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float* xr = &S.X[kr * kXStride + 8 * kc];
+    *reinterpret_cast<float4*>(xr) =
+        make_float4(__low2float(b2[0]), __high2float(b2[0]), __low2float(b2[1]), __high2float(b2[1]));
+    *reinterpret_cast<float4*>(xr + 4) =
+        make_float4(__low2float(b2[2]), __high2float(b2[2]), __low2float(b2[3]), __high2float(b2[3]));
+  }
+  __syncthreads();
+  if (tid < kHeadDim) {
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPage; ++k) sum += S.X[k * kXStride + tid];
+    S.mu[tid] = sum * (1.f / kPage);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) S.X[kr * kXStride + 8 * kc + e] -= S.mu[8 * kc + e];
+  __syncthreads();
+
+  // ---- 2. Gram entry (kr, kc), W = I
+  {
+    float g = 0.f;
+    for (int d = 0; d < kHeadDim; d += 4) {
+      const float4 xi = *reinterpret_cast<const float4*>(&S.X[kr * kXStride + d]);
+      const float4 xj = *reinterpret_cast<const float4*>(&S.X[kc * kXStride + d]);
+      g = fmaf(xi.x, xj.x, g);
+      g = fmaf(xi.y, xj.y, g);
+      g = fmaf(xi.z, xj.z, g);
+      g = fmaf(xi.w, xj.w, g);
+    }
+    S.G[0][tid] = g;
+    S.W[0][tid] = kr == kc ? 1.f : 0.f;
+  }
+  __syncthreads();
+  // round 0's rotations, from the Gram matrix; lane j keeps (c, signed s)
+  // of index j's pair in my_cs for the next round's pivots
+  float2 my_cs = make_float2(1.f, 0.f);
+  if (rot) {
+    const int q = jacobi_partner(j, 0);
+    const int lo = min(j, q), hi = max(j, q);
+    const float2 cs = jacobi_cs(S.G[0][lo * kPage + lo], S.G[0][hi * kPage + hi], S.G[0][lo * kPage + hi]);
+    my_cs = make_float2(cs.x, j == lo ? -cs.y : cs.y);
+    if (lane < kPage) S.cs[0][j] = my_cs;
+  }
+  __syncthreads();
+
+  // ---- 3. Jacobi: kSweeps sweeps of 15 rounds.  One CTA barrier a round
+  // hands the next (c, s) to the blocks; every group loads its next round's
+  // operands before it, as soon as its own group has stored them, so after
+  // it only the (c, s) remain to be read.  The rotation warp's pivot
+  // operands come from the G blocks (named barrier 1: the two G warps
+  // arrive, the rotation warp waits) and its current rotations from its own
+  // lanes; the G warps sync among themselves on barrier 2, the W warps on 3.
+  uint4 op = rot ? S.sched_p[0][j] : make_uint4(0, 0, 0, 0);
+  float gv[12];   // rotation lanes: G at the 12 operand positions of this round's pivots
+                  // G blocks: gv[0..3] = the block; W: gv[0..1] = the row's pair
+  int pr = 0, pc = 0;   // this round's row / column pair of the block (lo | hi << 8)
+#pragma unroll
+  for (int q = 0; q < 12; ++q) gv[q] = 0.f;
+  if (rot) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      gv[q] = S.G[0][(op.x >> (8 * q)) & 0xFF];
+      gv[4 + q] = S.G[0][(op.y >> (8 * q)) & 0xFF];
+      gv[8 + q] = S.G[0][(op.z >> (8 * q)) & 0xFF];
+    }
+  } else if (gblk) {
+    pr = S.pairs[0][gb >> 3];
+    pc = S.pairs[0][gb & 7];
+    const int r = pr & 0xFF, rp = pr >> 8, c = pc & 0xFF, cq = pc >> 8;
+    gv[0] = S.G[0][r * kPage + c];
+    gv[1] = S.G[0][r * kPage + cq];
+    gv[2] = S.G[0][rp * kPage + c];
+    gv[3] = S.G[0][rp * kPage + cq];
+  } else if (wblk) {
+    pc = S.pairs[0][wb & 7];
+    gv[0] = S.W[0][(wb >> 3) * kPage + (pc & 0xFF)];
+    gv[1] = S.W[0][(wb >> 3) * kPage + (pc >> 8)];
+  }
+  for (int it = 0, R = 0; it < kPbRounds; ++it) {
+    const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
+    const float2* cs = S.cs[cur];
+    if (rot) {
+      // the next round's pivots from this round's rotations, then its rotation
+      const int lo = op.w & 0xFF, hi = (op.w >> 8) & 0xFF;
+      float2 clo, chi;
+      clo.x = __shfl_sync(0xffffffffu, my_cs.x, lo);
+      clo.y = __shfl_sync(0xffffffffu, my_cs.y, lo);
+      chi.x = __shfl_sync(0xffffffffu, my_cs.x, hi);
+      chi.y = __shfl_sync(0xffffffffu, my_cs.y, hi);
+      auto entry = [&](const float* v, float2 cx, float2 cy) {
+        return rot_signed(cy.x, cy.y, rot_signed(cx.x, cx.y, v[0], v[1]), rot_signed(cx.x, cx.y, v[2], v[3]));
+      };
+      const float a = entry(gv, clo, clo);
+      const float bb = entry(gv + 4, chi, chi);
+      const float e = entry(gv + 8, clo, chi);
+      op = S.sched_p[Rn][j];
+      const float2 rt = jacobi_cs(a, bb, e);
+      my_cs = make_float2(rt.x, j == lo ? -rt.y : rt.y);
+      if (lane < kPage) S.cs[cur ^ 1][j] = my_cs;
+      // the next round's operands, once the G blocks have stored this round
+      asm volatile("bar.sync 1, 96;" ::: "memory");
+      const float* Gn = S.G[cur ^ 1];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gv[q] = Gn[(op.x >> (8 * q)) & 0xFF];
+        gv[4 + q] = Gn[(op.y >> (8 * q)) & 0xFF];
+        gv[8 + q] = Gn[(op.z >> (8 * q)) & 0xFF];
+      }
+    } else if (gblk) {
+      // block rows (r, rp) x columns (c, cp): rows rotated, then columns;
+      // index rp's signed s is the negation of index r's
+      const int r = pr & 0xFF, rp = pr >> 8, c = pc & 0xFF, cq = pc >> 8;
+      const float2 cr = cs[r], cc = cs[c];
+      const float a00 = rot_signed(cr.x, cr.y, gv[0], gv[2]), a01 = rot_signed(cr.x, cr.y, gv[1], gv[3]);
+      const float a10 = rot_signed(cr.x, -cr.y, gv[2], gv[0]), a11 = rot_signed(cr.x, -cr.y, gv[3], gv[1]);
+      float* Gn = S.G[cur ^ 1];
+      Gn[r * kPage + c] = rot_signed(cc.x, cc.y, a00, a01);
+      Gn[r * kPage + cq] = rot_signed(cc.x, -cc.y, a01, a00);
+      Gn[rp * kPage + c] = rot_signed(cc.x, cc.y, a10, a11);
+      Gn[rp * kPage + cq] = rot_signed(cc.x, -cc.y, a11, a10);
+      asm volatile("bar.arrive 1, 96;" ::: "memory");
+      pr = S.pairs[Rn][gb >> 3];
+      pc = S.pairs[Rn][gb & 7];
+      asm volatile("bar.sync 2, 64;" ::: "memory");
+      const int r2 = pr & 0xFF, rp2 = pr >> 8, c2 = pc & 0xFF, cq2 = pc >> 8;
+      gv[0] = Gn[r2 * kPage + c2];
+      gv[1] = Gn[r2 * kPage + cq2];
+      gv[2] = Gn[rp2 * kPage + c2];
+      gv[3] = Gn[rp2 * kPage + cq2];
+    } else if (wblk) {
+      const int row = wb >> 3, c = pc & 0xFF, cq = pc >> 8;
+      const float2 cc = cs[c];
+      float* Wn = S.W[cur ^ 1];
+      Wn[row * kPage + c] = rot_signed(cc.x, cc.y, gv[0], gv[1]);
+      Wn[row * kPage + cq] = rot_signed(cc.x, -cc.y, gv[1], gv[0]);
+      pc = S.pairs[Rn][wb & 7];
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+      gv[0] = Wn[row * kPage + (pc & 0xFF)];
+      gv[1] = Wn[row * kPage + (pc >> 8)];
+    }
+    R = Rn;
+    __syncthreads();
+  }
+  const float* Gf = S.G[kPbRounds & 1];
+  const float* Wf = S.W[kPbRounds & 1];
+
+  // ---- 4. rank the eigenvalues, top r, signs (warp 0; lanes 16..31 mirror 0..15)
+  if (warp == 0) {
+    const int i = lane & 15;
+    float lam[kPage];
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) {
+      const float v = Gf[j * kPage + j];
+      lam[j] = v == v ? v : -INFINITY;
+    }
+    const float vi = Gf[i * kPage + i];
+    const float my_lam = vi == vi ? vi : -INFINITY;
+    int pos = 0;
+    float lam1 = lam[0];
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) {
+      pos += (lam[j] > my_lam) || (lam[j] == my_lam && j < i);
+      lam1 = fmaxf(lam1, lam[j]);
+    }
+    if (lane < kPage) S.order[pos] = i;
+    float tail = pos >= kRank ? fmaxf(my_lam, 0.f) : 0.f;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) tail += __shfl_xor_sync(0xffffffffu, tail, o);
+    if (lane == 0) S.tail = tail;
+    __syncwarp();
+    if (lane < kRank) {
+      const int ev = S.order[lane];
+      const float l = Gf[ev * kPage + ev];
+      const bool keep = l > 1e-6f * lam1 && l > 0.f;
+      float best = -1.f, sgn = 1.f;
+#pragma unroll
+      for (int k = 0; k < kPage; ++k) {
+        const float v = Wf[k * kPage + ev];
+        if (fabsf(v) > best) {
+          best = fabsf(v);
+          sgn = v < 0.f ? -1.f : 1.f;
+        }
+      }
+      const float sig = keep ? sqrtf(l) : 0.f;
+      const float inv = keep ? 1.f / sig : 0.f;
+#pragma unroll
+      for (int k = 0; k < kPage; ++k) {
+        const float v = Wf[k * kPage + ev] * sgn;
+        S.lift[k * kRank + lane] = v * inv;
+        S.coef[k * kRank + lane] = v * sig;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 5. V = X^T W_r Lambda^{-1/2}: thread t < 256 -> dim t / 2, directions 4 (t % 2) ..
+  float v4[4] = {0.f, 0.f, 0.f, 0.f};
+  const int vdim = tid >> 1, k0 = 4 * (tid & 1);
+  if (tid < kPage * kPage) {
+#pragma unroll
+    for (int k = 0; k < kPage; ++k) {
+      const float x = S.X[k * kXStride + vdim];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) v4[m] = fmaf(x, S.lift[k * kRank + k0 + m], v4[m]);
+    }
+  }
+
+  // ---- 6. scales (block maxima), codes, packing
+  float vmax = 0.f, mmax = 0.f, cmax = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) vmax = fmaxf(vmax, fabsf(v4[m]));
+  if (tid < kHeadDim) mmax = fabsf(S.mu[tid]);
+  if (tid < kPage * kRank) cmax = fabsf(S.coef[tid]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+  }
+  if (lane == 0) {
+    S.red[0][warp] = vmax;
+    S.red[1][warp] = mmax;
+    S.red[2][warp] = cmax;
+  }
+  __syncthreads();
+  vmax = mmax = cmax = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPbWarps; ++w) {
+    vmax = fmaxf(vmax, S.red[0][w]);
+    mmax = fmaxf(mmax, S.red[1][w]);
+    cmax = fmaxf(cmax, S.red[2][w]);
+  }
+  const float sV = vmax / 7.f, sM = mmax / 127.f, sC = cmax / 127.f;
+  const float iV = sV > 0.f ? __frcp_rn(sV) : 0.f;
+  const float iM = sM > 0.f ? __frcp_rn(sM) : 0.f;
+  const float iC = sC > 0.f ? __frcp_rn(sC) : 0.f;
+  if (tid < kPage * kPage) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      int code = __float2int_rn(v4[m] * iV);
+      code = max(-7, min(7, code));
+      S.vcode[(k0 + m) * kHeadDim + vdim] = (int8_t)code;
+    }
+  }
+  if (tid < kHeadDim) {
+    int code = __float2int_rn(S.mu[tid] * iM);
+    code = max(-127, min(127, code));
+    S.rec[rec_mu_byte(tid)] = (uint8_t)(int8_t)code;
+  }
+  if (tid < kPage * kRank) {
+    int code = __float2int_rn(S.coef[tid] * iC);
+    code = max(-127, min(127, code));
+    S.rec[rec_coef_byte(tid / kRank, tid % kRank)] = (uint8_t)(int8_t)code;
+  }
+  if (tid == 0) {
+    float* scl = reinterpret_cast<float*>(&S.rec[768]);
+    scl[0] = sV;
+    scl[1] = sM;
+    scl[2] = sC;
+    scl[3] = S.tail;
+  }
+  __syncthreads();
+  if (tid < kRank * kHeadDim / 8) {   // basis word tid
+    const int k = tid >> 4;
+    uint32_t word = 0;
+#pragma unroll
+    for (int pos = 0; pos < 8; ++pos)
+      word |= ((uint32_t)S.vcode[k * kHeadDim + basis_word_dim(tid, pos)] & 0xFu) << (4 * pos);
+    *reinterpret_cast<uint32_t*>(&S.rec[4 * tid]) = word;
+  }
+  __syncthreads();
+  if (tid < kRecord / 16)
+    reinterpret_cast<uint4*>(p.summ + (blk * p.H_kv + h) * (int64_t)kRecord)[tid] =
+        reinterpret_cast<const uint4*>(S.rec)[tid];
+}
+
+cudaError_t launch_build_pages(const BuildParams& p, cudaStream_t stream) {
+  const int64_t grid = (int64_t)p.n_build * p.H_kv;
+  if (grid == 0) return cudaSuccess;
+  build_page_kernel<<<(unsigned)grid, kPbThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- fp32 records

@@ -287,6 +287,20 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// Single-instruction approximate reciprocal and reciprocal square root
+// (flush-to-zero forms: callers pass normal, positive-range operands).
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_rsqrt(float x) {
+  float y;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

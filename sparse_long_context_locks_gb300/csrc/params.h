@@ -96,6 +96,8 @@ int select16_max_clusters(size_t dyn, bool staged);
 cudaError_t launch_attn(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p,
                         cudaStream_t stream);
 cudaError_t launch_build(const BuildParams& p, cudaStream_t stream);
+// the same records from one CTA a page-head: for a step's few new pages
+cudaError_t launch_build_pages(const BuildParams& p, cudaStream_t stream);
 // unquantised fp32 records of rank r <= 16 (cfg quant = 0)
 cudaError_t launch_build_debug(const BuildParams& p, int rank_r, cudaStream_t stream);
 cudaError_t launch_score_debug(const ScoreParams& p, int rank_r, cudaStream_t stream);

@@ -169,3 +169,36 @@ def test_decode_step_crossing_in_a_graph_replays():
         assert torch.equal(summ, ref)
         assert torch.equal(bufs.out, first)
     assert L.locks_read_status(bufs.workspace) == 0
+
+
+def test_build_pending_special_pages_equal_the_bulk_build():
+    """The few-page builder (one CTA a page-head) must write the bulk
+    builder's records bit for bit: equal keys, exact low rank, a zero page,
+    large and tiny magnitudes, repeated eigenvalues, and random pages."""
+    rng = np.random.default_rng(12)
+    pages = [np.tile(rng.normal(size=128), (16, 1)),
+             rng.integers(-3, 4, 128) + rng.integers(-3, 4, (16, 3)) @ rng.integers(-2, 3, (128, 3)).T,
+             np.zeros((16, 128)),
+             rng.normal(size=(16, 128)) * 300.0,
+             rng.normal(size=(16, 128)) * 1e-3]
+    Q, _ = np.linalg.qr(rng.normal(size=(128, 16)))
+    pages.append(Q[:, :16].T * 2.0)                                       # 16 equal eigenvalues
+    pages.append(np.diag(np.repeat([4.0, 2.0], 8)) @ Q[:, :16].T)        # two repeated eigenvalues
+    pages.append(rng.normal(size=(16, 128)) * 3.0 + 5.0)                # a large centroid
+    for s in (0.05, 1.0, 30.0):
+        pages += [rng.normal(size=(16, 128)) * s for _ in range(8)]
+    K = torch.tensor(np.stack(pages), dtype=torch.bfloat16)              # 32 pages
+    for H in (1, 2):
+        kc = K.view(-1, H, 16, 128).contiguous().cuda()
+        nblk = kc.shape[0]
+        ids = torch.arange(nblk, dtype=torch.int32, device="cuda")
+        ref = torch.zeros(nblk, H, 784, dtype=torch.uint8, device="cuda")
+        got = torch.zeros_like(ref)
+        ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        L.locks_build_summaries(H, kc, ids, ref, ws)
+        n = torch.full((1,), nblk, dtype=torch.int32, device="cuda")
+        L.locks_build_pending(H, kc, ids, n, got, ws)
+        torch.cuda.synchronize()
+        assert L.locks_read_status(ws) == 0
+        diff = (got != ref).any(dim=-1).nonzero().tolist()
+        assert not diff, f"H={H}: records differ at (block, head) {diff[:8]}"
