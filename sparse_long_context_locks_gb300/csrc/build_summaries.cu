@@ -58,22 +58,31 @@ __host__ __device__ constexpr int jacobi_partner(int i, int r) {
 __device__ __forceinline__ float rot_lo(float c, float s, float x, float y) { return __fmaf_rn(c, x, __fmul_rn(-s, y)); }
 __device__ __forceinline__ float rot_hi(float c, float s, float x, float y) { return __fmaf_rn(c, x, __fmul_rn(s, y)); }
 
-// (c, s) of the rotation that zeroes e in [[a, e], [e, b]].  Approximate
-// reciprocal and square root (single instructions: this is the serial part of
-// every round): c and s are renormalised from t, so the rotation stays
-// orthogonal whatever t's rounding.  Every operand of those instructions is a
-// normal float (|2e| > 2e-30; 1 + tau^2, 1 + t^2 and |tau| + sqrt(1 + tau^2)
-// are at least 1).
+// (c, s) of the rotation that zeroes e in [[a, e], [e, b]] (the smaller of
+// the two, |theta| <= pi/4), from the half-angle relations with d = b - a,
+// f = 2e and h = sqrt(d^2 + f^2):
+//   c^2 = (1 + |d| / h) / 2,   s = sign(d) f / (2 h c).
+// Two dependent approximate reciprocal square roots (single instructions: the
+// rotation is the serial part of every round).  d and f are first scaled by
+// the power of two that brings |f| into [2, 4), and |d| is clamped to 2^60
+// (where s < 2^-58, a rotation the fp32 updates cannot tell from none): h^2
+// then lies in [4, 2^121] whatever the magnitudes of the page's keys, so both
+// operands stay normal.
 __device__ __forceinline__ float2 jacobi_cs(float a, float bb, float e) {
   float c = 1.f, s = 0.f;
   if (fabsf(e) > 1e-30f && __fmul_rn(e, e) > __fmul_rn(1e-24f, fabsf(__fmul_rn(a, bb)))) {
-    // |tau| beyond 1e18 gives a rotation below 1e-18: clamped so 1 + tau^2
-    // stays finite
-    const float tau = fminf(fmaxf(__fmul_rn(__fsub_rn(bb, a), fast_rcp(2.f * e)), -1e18f), 1e18f);
-    const float r2 = __fmaf_rn(tau, tau, 1.f);
-    const float t = copysignf(fast_rcp(__fmaf_rn(r2, fast_rsqrt(r2), fabsf(tau))), tau);
-    c = fast_rsqrt(__fmaf_rn(t, t, 1.f));
-    s = __fmul_rn(t, c);
+    const float d = __fsub_rn(bb, a);
+    // k = 2^-(exponent of e): |e| k in [1, 2)
+    const float k = __int_as_float(0x7F000000 - (__float_as_int(e) & 0x7F800000));
+    const float fk = __fmul_rn(__fmul_rn(2.f, e), k);                 // exact: f scaled into [2, 4)
+    const float ad = fminf(__fmul_rn(fabsf(d), k), 0x1p60f);
+    const float h2 = __fmaf_rn(ad, ad, __fmul_rn(fk, fk));
+    const float r = fast_rsqrt(h2);                                  // 1 / h
+    const float c2 = __fmaf_rn(__fmul_rn(0.5f, ad), r, 0.5f);       // in [0.5, 1]
+    const float sr = __fmul_rn(__fmul_rn(d < 0.f ? -0.5f : 0.5f, fk), r);
+    const float q = fast_rsqrt(c2);                                  // 1 / c
+    c = __fmul_rn(c2, q);
+    s = __fmul_rn(sr, q);
   }
   return make_float2(c, s);
 }
@@ -554,13 +563,17 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
   }
   __syncthreads();
 
-  // ---- 3. Jacobi: kSweeps sweeps of 15 rounds.  One CTA barrier a round
-  // hands the next (c, s) to the blocks; every group loads its next round's
-  // operands before it, as soon as its own group has stored them, so after
-  // it only the (c, s) remain to be read.  The rotation warp's pivot
-  // operands come from the G blocks (named barrier 1: the two G warps
-  // arrive, the rotation warp waits) and its current rotations from its own
-  // lanes; the G warps sync among themselves on barrier 2, the W warps on 3.
+  // ---- 3. Jacobi: kSweeps sweeps of 15 rounds, with no CTA-wide barrier in
+  // the loop.  Named barriers pass each hand-off:
+  //   1 (rotation warp waits; G and W warps arrive): round R's blocks have
+  //     stored G and W and read the round's (c, s);
+  //   4 (rotation warp arrives; G and W warps wait): the next round's (c, s)
+  //     are stored; the rotation warp releases them only after barrier 1, so
+  //     no warp can arrive at 1 for a round before 1 has completed the last;
+  //   2 (G warps) and 3 (W warps): a group's stores of a round are complete,
+  //     so it can load its operands of the next round before barrier 4.
+  // The rotation warp keeps its own lanes' rotations and loads the G entries
+  // of its next pivots once barrier 1 has passed.
   uint4 op = rot ? S.sched_p[0][j] : make_uint4(0, 0, 0, 0);
   float gv[12];   // rotation lanes: G at the 12 operand positions of this round's pivots
                   // G blocks: gv[0..3] = the block; W: gv[0..1] = the row's pair
@@ -587,17 +600,15 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
     gv[0] = S.W[0][(wb >> 3) * kPage + (pc & 0xFF)];
     gv[1] = S.W[0][(wb >> 3) * kPage + (pc >> 8)];
   }
-  for (int it = 0, R = 0; it < kPbRounds; ++it) {
-    const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
-    const float2* cs = S.cs[cur];
-    if (rot) {
+  if (rot) {
+    for (int it = 0, R = 0; it < kPbRounds; ++it) {
+      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
       // the next round's pivots from this round's rotations, then its rotation
+      // j is lo or hi: the other index's rotation comes from its lane
       const int lo = op.w & 0xFF, hi = (op.w >> 8) & 0xFF;
-      float2 clo, chi;
-      clo.x = __shfl_sync(0xffffffffu, my_cs.x, lo);
-      clo.y = __shfl_sync(0xffffffffu, my_cs.y, lo);
-      chi.x = __shfl_sync(0xffffffffu, my_cs.x, hi);
-      chi.y = __shfl_sync(0xffffffffu, my_cs.y, hi);
+      const float2 other = make_float2(__shfl_sync(0xffffffffu, my_cs.x, lo + hi - j),
+                                       __shfl_sync(0xffffffffu, my_cs.y, lo + hi - j));
+      const float2 clo = j == lo ? my_cs : other, chi = j == lo ? other : my_cs;
       auto entry = [&](const float* v, float2 cx, float2 cy) {
         return rot_signed(cy.x, cy.y, rot_signed(cx.x, cx.y, v[0], v[1]), rot_signed(cx.x, cx.y, v[2], v[3]));
       };
@@ -607,9 +618,10 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
       op = S.sched_p[Rn][j];
       const float2 rt = jacobi_cs(a, bb, e);
       my_cs = make_float2(rt.x, j == lo ? -rt.y : rt.y);
+      // (the buffer's previous round was read before barrier 1 of the last round)
       if (lane < kPage) S.cs[cur ^ 1][j] = my_cs;
-      // the next round's operands, once the G blocks have stored this round
-      asm volatile("bar.sync 1, 96;" ::: "memory");
+      asm volatile("bar.sync 1, 224;" ::: "memory");   // round R's blocks are done
+      if (it + 1 < kPbRounds) asm volatile("bar.arrive 4, 224;" ::: "memory");
       const float* Gn = S.G[cur ^ 1];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -617,11 +629,16 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
         gv[4 + q] = Gn[(op.y >> (8 * q)) & 0xFF];
         gv[8 + q] = Gn[(op.z >> (8 * q)) & 0xFF];
       }
-    } else if (gblk) {
+      R = Rn;
+    }
+  } else if (gblk) {
+    for (int it = 0, R = 0; it < kPbRounds; ++it) {
+      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
+      if (it > 0) asm volatile("bar.sync 4, 224;" ::: "memory");   // this round's (c, s)
       // block rows (r, rp) x columns (c, cp): rows rotated, then columns;
       // index rp's signed s is the negation of index r's
       const int r = pr & 0xFF, rp = pr >> 8, c = pc & 0xFF, cq = pc >> 8;
-      const float2 cr = cs[r], cc = cs[c];
+      const float2 cr = S.cs[cur][r], cc = S.cs[cur][c];
       const float a00 = rot_signed(cr.x, cr.y, gv[0], gv[2]), a01 = rot_signed(cr.x, cr.y, gv[1], gv[3]);
       const float a10 = rot_signed(cr.x, -cr.y, gv[2], gv[0]), a11 = rot_signed(cr.x, -cr.y, gv[3], gv[1]);
       float* Gn = S.G[cur ^ 1];
@@ -629,7 +646,7 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
       Gn[r * kPage + cq] = rot_signed(cc.x, -cc.y, a01, a00);
       Gn[rp * kPage + c] = rot_signed(cc.x, cc.y, a10, a11);
       Gn[rp * kPage + cq] = rot_signed(cc.x, -cc.y, a11, a10);
-      asm volatile("bar.arrive 1, 96;" ::: "memory");
+      asm volatile("bar.arrive 1, 224;" ::: "memory");
       pr = S.pairs[Rn][gb >> 3];
       pc = S.pairs[Rn][gb & 7];
       asm volatile("bar.sync 2, 64;" ::: "memory");
@@ -638,20 +655,26 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
       gv[1] = Gn[r2 * kPage + cq2];
       gv[2] = Gn[rp2 * kPage + c2];
       gv[3] = Gn[rp2 * kPage + cq2];
-    } else if (wblk) {
+      R = Rn;
+    }
+  } else if (wblk) {
+    for (int it = 0, R = 0; it < kPbRounds; ++it) {
+      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
+      if (it > 0) asm volatile("bar.sync 4, 224;" ::: "memory");
       const int row = wb >> 3, c = pc & 0xFF, cq = pc >> 8;
-      const float2 cc = cs[c];
+      const float2 cc = S.cs[cur][c];
       float* Wn = S.W[cur ^ 1];
       Wn[row * kPage + c] = rot_signed(cc.x, cc.y, gv[0], gv[1]);
       Wn[row * kPage + cq] = rot_signed(cc.x, -cc.y, gv[1], gv[0]);
+      asm volatile("bar.arrive 1, 224;" ::: "memory");
       pc = S.pairs[Rn][wb & 7];
       asm volatile("bar.sync 3, 128;" ::: "memory");
       gv[0] = Wn[row * kPage + (pc & 0xFF)];
       gv[1] = Wn[row * kPage + (pc >> 8)];
+      R = Rn;
     }
-    R = Rn;
-    __syncthreads();
   }
+  __syncthreads();
   const float* Gf = S.G[kPbRounds & 1];
   const float* Wf = S.W[kPbRounds & 1];
 
