@@ -60,12 +60,19 @@ __device__ __forceinline__ void unit_items(const AttnParams& p, int b, int h, in
   items = nsel + (t > 0 ? 1 : 0);
 }
 
+// Entry i of the unit's selection list, read before the list's length is
+// known (entries past the length are never used); -1 past the budget.
+__device__ __forceinline__ int sel_entry(const AttnParams& p, int b, int h, int i) {
+  return (!p.dense && i >= 0 && i < p.budget) ? p.selected[((int64_t)b * p.H_kv + h) * p.budget + i] : -1;
+}
+
 // Resolve item i of the unit: physical block (or -1 to skip) and valid tokens.
+// sel_i: the unit's selection entry i (sel_entry), for i < nsel.
 __device__ __forceinline__ void item_block(const AttnParams& p, int b, int h, int i, int n, int t,
-                                           int nsel, int64_t& blk, int& valid) {
+                                           int nsel, int sel_i, int64_t& blk, int& valid) {
   int page;
   if (i < nsel) {
-    page = p.dense ? i : p.selected[((int64_t)b * p.H_kv + h) * p.budget + i];
+    page = p.dense ? i : sel_i;
     valid = kPage;
     if (page < 0 || page >= n) {
       flag_status(p.status, LOCKS_FLAG_BAD_SELECT);
@@ -133,6 +140,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   // visible from here on
   griddep_wait();
 
+  // The first two windows' selection entries are requested together with the
+  // request's length and the list's length: one dependent round trip fewer
+  // before the first block lookup.  (A split's items start at
+  // split * items_per_split whatever the unit's item count.)
+  const int spec0 = split * p.items_per_split + warp + lane * kAttnWarps;
+  const int sel0 = sel_entry(p, b, h, spec0), sel1 = sel_entry(p, b, h, spec0 + 32 * kAttnWarps);
   int n, tail, nsel, items;
   unit_items(p, b, h, n, tail, nsel, items);
   const int r0 = min(items, split * p.items_per_split);
@@ -147,9 +160,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   int64_t cur_blk = -1, nxt_blk = -1;
   int cur_valid = 0, nxt_valid = 0;
   if (lane < my_count)
-    item_block(p, b, h, my_first + lane * kAttnWarps, n, tail, nsel, cur_blk, cur_valid);
+    item_block(p, b, h, my_first + lane * kAttnWarps, n, tail, nsel, sel0, cur_blk, cur_valid);
   if (32 + lane < my_count)
-    item_block(p, b, h, my_first + (32 + lane) * kAttnWarps, n, tail, nsel, nxt_blk, nxt_valid);
+    item_block(p, b, h, my_first + (32 + lane) * kAttnWarps, n, tail, nsel, sel1, nxt_blk, nxt_valid);
 
   auto issue = [&](int64_t blk, int stage) {
     attn_issue_page(&tmk, &tmv, ring_ptr + stage * kStageBytes, &mybar[stage], blk, p.H_kv, h);
@@ -187,8 +200,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         cur_valid = nxt_valid;
         nxt_blk = -1;
         nxt_valid = 0;
-        if (kn + 32 + lane < my_count)
-          item_block(p, b, h, my_first + (kn + 32 + lane) * kAttnWarps, n, tail, nsel, nxt_blk, nxt_valid);
+        if (kn + 32 + lane < my_count) {
+          const int i = my_first + (kn + 32 + lane) * kAttnWarps;
+          item_block(p, b, h, i, n, tail, nsel, sel_entry(p, b, h, i), nxt_blk, nxt_valid);
+        }
       }
       const int64_t blk = __shfl_sync(0xffffffffu, cur_blk, kn & 31);
       const int v = __shfl_sync(0xffffffffu, cur_valid, kn & 31);
