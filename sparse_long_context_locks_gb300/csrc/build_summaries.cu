@@ -432,9 +432,10 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 // 2 each own 32 of them and apply the round's rotations (rows, then
 // columns); warps 3, 5, 6 and 7 rotate W's column pairs, one (row, pair) a
 // thread; warp 0's lanes, alone on their SM sub-partition (warps w and w + 4
-// share one; warp 4 only keeps the barriers), form the three entries of the
-// next round's pivots from the same G and rotations and take the next
-// round's (c, s), so they are ready at the one barrier a round.  Blocks keep
+// share one; warp 4 only keeps the final barrier), form the three entries of
+// the next round's pivots from the same G and rotations and take the next
+// round's (c, s) while the blocks apply this round's; named barriers hand
+// each round's results on (no CTA-wide barrier in the loop).  Blocks keep
 // the shared-memory traffic of a round low: the pivots' loads are on the
 // critical path and share the load pipe with the blocks'.  Every step
 // (centroid, Gram, rotations, ranking, lift, quantisation) uses the same
