@@ -18,6 +18,12 @@
  *    never allocates, frees or synchronises inside the decode entry points, so
  *    a sequence of calls can be captured into a CUDA graph.  Every call is
  *    asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *    One exception: `out` (the attention result) may also be page-locked host
+ *    memory that the device addresses with the same pointer (cudaHostAlloc'd
+ *    memory under unified addressing; locks_device_accessible() says whether
+ *    a pointer qualifies).  The kernels then store the result straight into
+ *    host memory (on a Grace system, over NVLink-C2C), and the caller reads
+ *    it once `stream` has completed: no separate device-to-host copy.
  *  - All device pointers must be 16-byte aligned.
  *  - Host-side validation runs before any launch; on failure nothing is
  *    launched and an error code is returned.  A failed launch returns
@@ -139,6 +145,14 @@ locks_status locks_workspace_bytes(const locks_cfg *cfg, int32_t batch, int32_t 
  * tickets must start at zero; the kernels keep the tickets at zero after
  * every call).  Enqueues one memset on `stream`. */
 locks_status locks_workspace_init(void *workspace, size_t workspace_bytes, locks_stream_t stream);
+
+/* 1 when the current device's kernels can dereference p: device or managed
+ * memory, or page-locked host memory whose device pointer equals p (the
+ * form `out` may take); 0 otherwise, including NULL and pointers the CUDA
+ * runtime does not know (pageable host memory).  Host-side query, no launch
+ * and no synchronisation.  The paper has no counterpart: it is a check for
+ * callers that hand `out` in host memory. */
+int32_t locks_device_accessible(const void *p);
 
 /* Synchronise `stream`, copy the status word to *flags and clear it.
  * Returns LOCKS_ERR_TIMEOUT (with *flags written) when a bounded wait ran

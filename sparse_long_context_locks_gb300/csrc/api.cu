@@ -323,6 +323,24 @@ locks_status locks_read_status(void* workspace, uint32_t* flags, locks_stream_t 
   return (v & LOCKS_FLAG_TIMEOUT) ? LOCKS_ERR_TIMEOUT : LOCKS_OK;
 }
 
+int32_t locks_device_accessible(const void* p) {
+  if (p == nullptr) return 0;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();   // an unknown pointer leaves no sticky error
+    return 0;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return 1;
+    case cudaMemoryTypeHost:
+      return a.devicePointer == p ? 1 : 0;
+    default:
+      return 0;
+  }
+}
+
 locks_status locks_build_summaries(const locks_cfg* cfg, const void* k_cache, int64_t num_blocks,
                                    const int32_t* block_ids, int32_t n_build, void* summaries,
                                    void* workspace, size_t workspace_bytes, locks_stream_t stream) {

@@ -57,6 +57,7 @@ _SIGS = {
     "locks_workspace_bytes": (_I32, [_CFG, _I32, _I32, _I32, ctypes.POINTER(_SZ)]),
     "locks_workspace_init": (_I32, [_P, _SZ, _P]),
     "locks_read_status": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "locks_device_accessible": (_I32, [_P]),
     "locks_build_summaries": (_I32, [_CFG, _P, _I64, _P, _I32, _P, _P, _SZ, _P]),
     "locks_build_pending": (_I32, [_CFG, _P, _I64, _P, _P, _I32, _P, _P, _SZ, _P]),
     "locks_score": (_I32, [_CFG, _P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _SZ, _P]),
@@ -195,6 +196,23 @@ def _req(t, name: str, dtype: str, shape=None, optional: bool = False) -> None:
             raise ValueError(f"{name} must have shape {want_s}, got {list(t.shape)}")
 
 
+def _req_out(out, B: int, H: int) -> None:
+    """out [batch, H*G, 128] fp32: a CUDA tensor, or a pinned host tensor the
+    device addresses with the same pointer (the kernels then store the result
+    straight into host memory)."""
+    import torch
+    if isinstance(out, torch.Tensor) and not out.is_cuda:
+        if not out.is_pinned():
+            raise ValueError("out must be a CUDA tensor or a pinned host tensor")
+        if out.dtype != torch.float32 or not out.is_contiguous() or \
+                tuple(out.shape) != (B, H * GROUP, HEAD_DIM):
+            raise ValueError(f"out must be a contiguous float32 tensor of shape [{B}, {H * GROUP}, {HEAD_DIM}]")
+        if load().locks_device_accessible(out.data_ptr()) != 1:
+            raise ValueError("out: this pinned host memory is not addressable by the device")
+        return
+    _req(out, "out", "float32", (B, H * GROUP, HEAD_DIM))
+
+
 def _req_cache(t, name: str, H: int) -> None:
     _req(t, name, "bfloat16", (None, H, PAGE_SIZE, HEAD_DIM))
 
@@ -295,7 +313,7 @@ def locks_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
@@ -314,7 +332,7 @@ def locks_select_sparse_decode(num_kv_heads, q, k_cache, v_cache, block_table, s
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
@@ -334,7 +352,7 @@ def locks_decode_step(num_kv_heads, q, summaries, k_cache, v_cache, block_table,
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
@@ -357,7 +375,7 @@ def locks_decode_step_crossing(num_kv_heads, q, summaries, k_cache, v_cache, blo
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req(scores, "scores", "float32", (B, num_kv_heads, MP, GROUP), optional=True)
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads, quant=quant, rank=rank)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
@@ -374,7 +392,7 @@ def locks_dense_decode(num_kv_heads, q, k_cache, v_cache, block_table, seq_lens,
     B, MP = _req_step(num_kv_heads, q, block_table, seq_lens)
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     _req(workspace, "workspace", "uint8")
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
@@ -392,7 +410,7 @@ def locks_sparse_decode_noalloc(num_kv_heads, q, k_cache, v_cache, block_table, 
     _req_cache(k_cache, "k_cache", num_kv_heads)
     _req(v_cache, "v_cache", "bfloat16", tuple(k_cache.shape))
     _req_selection(num_kv_heads, B, budget_pages, selected, n_selected)
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     cfg = make_cfg(num_kv_heads)
     scale = 1.0 / math.sqrt(HEAD_DIM) if sm_scale is None else sm_scale
     _check(load().locks_sparse_decode_noalloc(
@@ -525,7 +543,7 @@ def locks_cp_sparse_decode_partial(num_kv_heads, q, k_cache, v_cache, block_tabl
 def locks_cp_merge_attention(num_kv_heads, states_all, out, stream=None):
     R, B = states_all.shape[0], states_all.shape[1]
     _req(states_all, "states_all", "float32", (R, B, num_kv_heads * GROUP, 2 + HEAD_DIM))
-    _req(out, "out", "float32", (B, num_kv_heads * GROUP, HEAD_DIM))
+    _req_out(out, B, num_kv_heads)
     cfg = make_cfg(num_kv_heads)
     _check(load().locks_cp_merge_attention(ctypes.byref(cfg), B, R, _ptr(states_all), _ptr(out),
                                            _stream(stream)), "locks_cp_merge_attention")

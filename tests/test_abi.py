@@ -36,6 +36,12 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= set(L._SIGS), "binding misses a declared entry point"
 
 
+def test_device_accessible_refuses_null_and_pageable_host_memory(lib):
+    assert lib.locks_device_accessible(None) == 0
+    buf = ctypes.create_string_buffer(4096)      # pageable host memory
+    assert lib.locks_device_accessible(ctypes.addressof(buf)) == 0
+
+
 def test_sizes_and_status_strings(lib):
     assert L.locks_summary_bytes(8) == 784
     # unquantised fp32 records: mu, V (128 x r), C (16 x r), tail + pad
