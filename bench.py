@@ -354,6 +354,48 @@ class WorkloadCase:
 
 
 # ------------------------------------------------------------------ main arm
+def selection_quality(w, data, selected, n_selected):
+    """How well the step's selection tracks the pages that carry the
+    attention mass (a reported figure, not a parity bar): per (request, KV
+    head), the share of the k pages with the largest exact masses -- every
+    key read, log-sum-exp over each page's keys per query head, normalised
+    per head and averaged over the group as the method averages its
+    estimates -- that the step selected, and the planted carrier pages it
+    kept next to those exact selection keeps.  Computed with torch on the
+    GPU after the timed region."""
+    import torch
+    H, G, k = w.num_kv_heads, w.group, w.budget_pages
+    lens = data["seq_lens"].cpu().tolist()
+    sel = selected.cpu()
+    nsel = n_selected.cpu()
+    carriers = {}
+    for (b, h, page, slot) in data["carriers"]:
+        carriers.setdefault((b, h), set()).add(page)
+    recalls, kept, kept_exact, n_car = [], 0, 0, 0
+    for b in range(w.batch):
+        n = lens[b] // 16
+        if n == 0:
+            continue
+        blocks = data["block_table"][b, :n].long()
+        for h in range(H):
+            K = data["k_cache"][blocks, h].float()                        # [n, 16, 128]
+            q = data["q"][b, h * G:(h + 1) * G].float()                   # [G, 128]
+            s = torch.logsumexp(torch.einsum("njd,gd->ngj", K, q) / math.sqrt(128), dim=-1)   # [n, G]
+            avg = torch.exp(s - torch.logsumexp(s, dim=0)).mean(dim=1)
+            kk = min(k, n)
+            exact = set(torch.topk(avg, kk).indices.cpu().tolist())
+            got = set(sel[b, h, :int(nsel[b, h])].tolist())
+            recalls.append(len(exact & got) / kk)
+            car = carriers.get((b, h), set())
+            n_car += len(car)
+            kept += len(car & got)
+            kept_exact += len(car & exact)
+    return {"recall_vs_exact_mass": sum(recalls) / len(recalls), "min_recall": min(recalls),
+            "units": len(recalls), "carriers": n_car, "carriers_kept": kept, "carriers_kept_by_exact": kept_exact,
+            "reading": "share of the top-k pages by exact attention mass (every key read) that the step "
+                       "selected; planted carrier pages kept, next to what exact selection keeps"}
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -592,6 +634,14 @@ def main():
     # decoding.
     n_layers = 32
     layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
+    # the selection of one step on the workload's own lengths (the rows above
+    # left the crossing lengths' selection in the buffers)
+    with torch.cuda.stream(stream):
+        L.locks_decode_step(H, data["q"], summ, data["k_cache"], data["v_cache"], data["block_table"],
+                            data["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
+                            bufs.workspace, scores=bufs.scores, stream=stream)
+    stream.synchronize()
+    quality = selection_quality(w, data, bufs.selected, bufs.n_selected) if rank == 0 else None
     layers32 = None
     if args.layers32 and torch.cuda.mem_get_info()[0] > n_layers * layer_bytes + (8 << 30):
         kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_layers)]
@@ -731,6 +781,7 @@ def main():
         "roofline": roofline,
         "roofline_kernels": kernels,
         "roofline_step": main_rows["roofline_step"],
+        "quality": quality,
         "rows": main_rows,
         "layers32": layers32,
         "workloads": others,
