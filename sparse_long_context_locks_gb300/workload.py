@@ -79,6 +79,11 @@ CONFIGS = {
     "batch64_256k_fullrank": Workload("batch64_256k_fullrank", batch=64, context=262144,
                                       num_kv_heads=8, group=4, budget_tokens=2048,
                                       carriers_per_head=8, key_regime="fullrank"),
+    # the batch-64 attention and selection shapes (512 units, 128 selected
+    # pages each: 537 MB of K/V a step) on a cache small enough (2.1 GB of K
+    # and V) for counter captures of single kernels
+    "batch64_8k": Workload("batch64_8k", batch=64, context=8192, num_kv_heads=8, group=4,
+                           budget_tokens=2048, carriers_per_head=4),
 }
 
 
