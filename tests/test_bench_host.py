@@ -80,3 +80,39 @@ def test_cpu_baseline_unit_runs_the_whole_oracle_path(tmp_path):
             secs, abs_sum = bench._oracle_unit((str(tmp_path), b, h, w.group, w.budget_pages))
             assert secs > 0
             assert abs_sum == float(np.abs(want[(b, h)]["out"]).sum())
+
+
+def test_selection_quality_against_the_oracles_exact_selection():
+    """bench.py's reported selection quality (torch, every key read) on a
+    tiny CPU workload: the oracle's exact-mass selection scores recall 1 and
+    keeps what it keeps; selecting the lowest pages instead scores the recall
+    of that set against the oracle's."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from sparse_long_context_locks_gb300 import workload as W
+    w = W.Workload("q", batch=2, context=16 * 40 + 3, context_hi=16 * 60, num_kv_heads=2, group=4,
+                   budget_tokens=16 * 8, carriers_per_head=3, seed=4)
+    d = W.generate(w, device="cpu")
+    H, G, k = w.num_kv_heads, w.group, w.budget_pages
+    sel = torch.full((w.batch, H, k), -1, dtype=torch.int32)
+    nsel = torch.zeros(w.batch, H, dtype=torch.int32)
+    low = torch.full_like(sel, -1)
+    exact_sets = {}
+    for b in range(w.batch):
+        n = int(d["seq_lens"][b]) // 16
+        blocks = d["block_table"][b, :n].long()
+        for h in range(H):
+            K = d["k_cache"][blocks, h].double().numpy()
+            q = d["q"][b, h * G:(h + 1) * G].double().numpy()
+            ex, _ = O.select_pages(O.exact_page_lse(q, K), k)
+            exact_sets[(b, h)] = set(ex.tolist())
+            sel[b, h, :len(ex)] = torch.from_numpy(ex.astype(np.int32))
+            nsel[b, h] = len(ex)
+            low[b, h, :len(ex)] = torch.arange(len(ex), dtype=torch.int32)
+    q1 = bench.selection_quality(w, d, sel, nsel)
+    assert q1["recall_vs_exact_mass"] == 1.0 and q1["min_recall"] == 1.0
+    assert q1["carriers_kept"] == q1["carriers_kept_by_exact"] and q1["carriers"] == w.batch * H * 3
+    q2 = bench.selection_quality(w, d, low, nsel)
+    want = np.mean([len(exact_sets[(b, h)] & set(range(k))) / k for b in range(w.batch) for h in range(H)])
+    assert abs(q2["recall_vs_exact_mass"] - want) < 1e-12
