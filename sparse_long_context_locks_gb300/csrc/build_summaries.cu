@@ -426,97 +426,354 @@ __global__ void __launch_bounds__(kBuildThreads) build_kernel(const BuildParams 
 
 // ---------------------------------------------------------------- a few pages
 // The pages a decode step completes are few (one a request), so their build
-// is bound by the latency of one page-head's Jacobi chain, not by
-// throughput.  build_page_kernel gives each page-head a CTA of 8 warps.  In a
-// round the 8 pairs split G into 64 2x2 blocks (r, rp) x (c, cp): warps 1 and
-// 2 each own 32 of them and apply the round's rotations (rows, then
-// columns); warps 3, 5, 6 and 7 rotate W's column pairs, one (row, pair) a
-// thread; warp 0's lanes, alone on their SM sub-partition (warps w and w + 4
-// share one; warp 4 only keeps the final barrier), form the three entries of
-// the next round's pivots from the same G and rotations and take the next
-// round's (c, s) while the blocks apply this round's; named barriers hand
-// each round's results on (no CTA-wide barrier in the loop).  Blocks keep
-// the shared-memory traffic of a round low: the pivots' loads are on the
-// critical path and share the load pipe with the blocks'.  Every step
-// (centroid, Gram, rotations, ranking, lift, quantisation) uses the same
-// operations in the same order as the half-warp build: the records are bit
-// for bit those of build_kernel.
+// is bound by the latency of one page-head's eigendecomposition, not by
+// throughput.  build_page_kernel gives each page-head a CTA of 8 warps and
+// decomposes G by Householder reduction, multisection and inverse iteration
+// (page_eigen_tridiag), whose dependency chain is about a third of the 120
+// Jacobi rounds'.  The loops stay rolled: a step's kernel runs with its code
+// out of L2, and straight-line code pays for every instruction fetched.  The
+// records meet the same bar as build_kernel's against the decomposition in
+// fp64 (codes within one of it), not the bits of build_kernel's.
 constexpr int kPbWarps = 8;
 constexpr int kPbThreads = kPbWarps * 32;
-constexpr int kPbRounds = kSweeps * 15;
 
 struct PageSmem {
   float X[kPage * kXStride];           // keys, then centred keys
-  float G[2][kPage * kPage];           // current / next
-  float W[2][kPage * kPage];
-  float2 cs[2][kPage];                 // (c, signed s) of the pair holding index j, this / next round
+  float G[2][kPage * kPage];           // G, then its eigenvalues on the diagonal; the reflectors
+  float W[2][kPage * kPage];           // the eigenvectors (columns); Gram-Schmidt scratch
   float mu[kHeadDim];
   float lift[kPage * kRank];
   float coef[kPage * kRank];
   int order[kPage];
-  // round R's pairs: lo | hi << 8 in pair k (ascending lo)
-  uint16_t pairs[15][8];
-  // rotation lane j, round R: the 12 word offsets of the next round's pivot
-  // entries' operands ((lo,lo), (plo,lo), (lo,plo), (plo,plo); the same for
-  // (hi,hi); (lo,hi), (plo,hi), (lo,phi), (plo,phi)) and the pair (lo, hi)
-  uint4 sched_p[15][kPage];
+  // tridiagonal matrix T (diagonal, subdiagonal), its eigenvalues, and the
+  // scale, bracket and norm of T
+  float tri_d[kPage], tri_e[kPage], tri_lam[kPage];
+  float tri_s[4];
   float red[3][kPbWarps];
   float tail;
   int8_t vcode[kRank * kHeadDim];
   __align__(16) uint8_t rec[kRecord];
 };
 
-// A rotation with the sign of s already chosen for the index it updates:
-// -s for the lower index of its pair (rot_lo), s for the higher (rot_hi).
-__device__ __forceinline__ float rot_signed(float c, float s_signed, float x, float y) {
-  return __fmaf_rn(c, x, __fmul_rn(s_signed, y));
-}
+static_assert(offsetof(PageSmem, G) % 16 == 0 && (kPage * kPage * sizeof(float)) % 16 == 0,
+              "the reflectors in G[1] are read as float4");
 
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-  return (uint32_t)a | (uint32_t)b << 8 | (uint32_t)c << 16 | (uint32_t)d << 24;
+// Eigenpairs of the symmetric 16x16 matrix in S.G[0] by Householder
+// tridiagonalisation, multisection on Sturm counts and inverse iteration,
+// the classical alternative to Jacobi (Golub & Van Loan §8.3 for the
+// tridiagonal reduction and Sturm sequences, §8.2 for inverse iteration).
+// All kPbThreads threads call it.  On return S.G[0][i][i] holds eigenvalue i
+// (ascending in i) and column i of S.W[0] its unit eigenvector.
+//
+// Built for latency, with three CTA barriers in all:
+//  * the reduction runs in warp 0's registers, lane l holding column l; the
+//    update keeps A symmetric bit for bit, so lane l's own element (k, l)
+//    is the reflector's component l and no lane needs another's row;
+//  * the tridiagonal matrix T is scaled by a power of two to a norm near 1,
+//    and the Sturm counts use the three-term recurrence of the leading
+//    minors (one fused multiply-add a step on the dependency chain, the
+//    minors rescaled by a power of two every fourth step), 16 points an
+//    eigenvalue a round;
+//  * the inverse iteration factors T - lambda I once and solves twice.
+__device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
+  float* HV = S.G[1];     // row k: unit Householder vector of step k
+  const int warp = tid >> 5, lane = tid & 31;
+  // ---- Householder: A = Q T Q^T, Q = H_0 H_1 ... H_13, H_k = I - 2 v_k v_k^T
+  if (warp == 0) {
+    const int l = lane & 15;
+    // column l of A (equal to row l); at step k register i holds row k + i,
+    // zero past row 15 (the rows shift down a register a step)
+    float a[kPage];
+#pragma unroll
+    for (int i = 0; i < kPage; ++i) a[i] = S.G[0][i * kPage + l];
+#pragma unroll 1
+    for (int k = 0; k < kPage - 2; ++k) {
+      float xs[kPage];   // column k, rows k, k + 1, ..
+#pragma unroll
+      for (int i = 0; i < kPage; ++i) xs[i] = __shfl_sync(0xffffffffu, a[i], k);
+      float sig0 = 0.f, sig1 = 0.f;   // below the subdiagonal entry
+#pragma unroll
+      for (int i = 2; i < kPage; ++i) {
+        if (i & 1) sig1 = fmaf(xs[i], xs[i], sig1);
+        else sig0 = fmaf(xs[i], xs[i], sig0);
+      }
+      const float sig = sig0 + sig1;
+      const float x0 = xs[1];
+      float alpha = x0, v0 = 0.f, inv = 0.f;
+      if (sig > 0.f) {
+        const float nrm = sqrtf(fmaf(x0, x0, sig));
+        alpha = x0 >= 0.f ? -nrm : nrm;
+        v0 = x0 - alpha;
+        inv = rsqrtf(fmaf(v0, v0, sig));
+      }
+      float v[kPage];
+      v[0] = 0.f;
+      v[1] = v0 * inv;
+#pragma unroll
+      for (int i = 2; i < kPage; ++i) v[i] = xs[i] * inv;
+      // this lane's component: element (k, l) of A equals (l, k)
+      const float vl = l == k + 1 ? v0 * inv : (l > k + 1 ? a[0] * inv : 0.f);
+      if (lane < kPage) HV[k * kPage + lane] = vl;
+      if (lane == 0) {
+        S.tri_d[k] = xs[0];
+        S.tri_e[k] = alpha;
+      }
+      // p = A v (row l of A is column l), then w = 2 p - 2 (v.p) v
+      float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+      for (int i = 1; i < kPage; ++i) {
+        if (i & 1) p1 = fmaf(a[i], v[i], p1);
+        else p0 = fmaf(a[i], v[i], p0);
+      }
+      const float pl = p0 + p1;
+      float pv[kPage];
+#pragma unroll
+      for (int i = 1; i < kPage; ++i) {
+        const float t = __shfl_sync(0xffffffffu, pl, k + i);
+        pv[i] = k + i < kPage ? t : 0.f;
+      }
+      float K0 = 0.f, K1 = 0.f;
+#pragma unroll
+      for (int i = 1; i < kPage; ++i) {
+        if (i & 1) K1 = fmaf(v[i], pv[i], K1);
+        else K0 = fmaf(v[i], pv[i], K0);
+      }
+      const float m2K = -2.f * (K0 + K1);
+      const float wl = fmaf(m2K, vl, 2.f * pl);
+      // A -= v w^T + w v^T on rows and columns past k: both products are
+      // rounded, then added, so elements (i, l) and (l, i) stay equal; row
+      // and column k are final (d_k, e_k) and drop out
+#pragma unroll
+      for (int i = 1; i < kPage; ++i) {
+        const float wi = fmaf(m2K, v[i], 2.f * pv[i]);
+        const float upd = __fadd_rn(__fmul_rn(v[i], wl), __fmul_rn(wi, vl));
+        a[i - 1] = l > k ? __fsub_rn(a[i], upd) : a[i];
+      }
+      a[kPage - 1] = 0.f;
+    }
+    const float d14 = __shfl_sync(0xffffffffu, a[0], 14);
+    const float d15 = __shfl_sync(0xffffffffu, a[1], 15);
+    const float e14 = __shfl_sync(0xffffffffu, a[1], 14);
+    if (lane == 0) {
+      S.tri_d[14] = d14;
+      S.tri_d[15] = d15;
+      S.tri_e[14] = e14;
+      S.tri_e[15] = 0.f;
+    }
+    __syncwarp();
+    // Gershgorin bracket of T, and the power of two that scales it to [1, 2)
+    const int i = l;
+    const float di = S.tri_d[i], ei = fabsf(S.tri_e[i]), em = i > 0 ? fabsf(S.tri_e[i - 1]) : 0.f;
+    float lo = di - ei - em, hi = di + ei + em;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+      const float bound = fmaxf(fabsf(lo), fabsf(hi));
+      const int ex = (__float_as_int(bound) >> 23) & 0xFF;
+      const float sc = bound > 1e-30f ? __int_as_float((254 - ex) << 23) : 1.f;   // bound * sc in [1, 2)
+      const float span = (hi - lo) * sc;
+      S.tri_s[0] = sc;
+      S.tri_s[1] = fmaf(lo, sc, -(1e-6f * span + 1e-30f));
+      S.tri_s[2] = fmaf(hi, sc, 1e-6f * span + 1e-30f);
+      S.tri_s[3] = bound;
+    }
+  }
+  __syncthreads();
+  // ---- multisection on the scaled T: half-warp i brackets eigenvalue i
+  // (ascending); lane t counts the eigenvalues below a + (t + 1)(b - a)/17
+  {
+    const int i = tid >> 4, t = tid & 15;
+    const float sc = S.tri_s[0];
+    float d[kPage], me2[kPage];   // scaled diagonal, minus the scaled squared subdiagonal
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) {
+      d[j] = S.tri_d[j] * sc;
+      const float ej = S.tri_e[j] * sc;
+      me2[j] = -ej * ej;
+    }
+    float a = S.tri_s[1], b = S.tri_s[2];
+#pragma unroll 1
+    for (int round = 0; round < 6; ++round) {
+      const float x = fmaf((b - a) * (1.f / 17.f), (float)(t + 1), a);
+      // leading minors P_j of T - x I: P_0 = 1, P_1 = d_0 - x,
+      // P_{j+1} = (d_j - x) P_j - e_{j-1}^2 P_{j-1}; a sign change from P_j
+      // to P_{j+1} is a negative pivot, one eigenvalue below x.  An exact
+      // zero takes the sign opposite to its predecessor's (a pivot of -0).
+      float Pp = 1.f, P = d[0] - x;
+      if (P == 0.f) P = -0x1p-120f;
+      int cnt = P < 0.f;
+#pragma unroll
+      for (int j = 1; j < kPage; ++j) {
+        float Pn = fmaf(d[j] - x, P, me2[j - 1] * Pp);
+        if (Pn == 0.f) Pn = P < 0.f ? 0x1p-120f : -0x1p-120f;
+        cnt += (Pn < 0.f) != (P < 0.f);
+        Pp = P;
+        P = Pn;
+        if ((j & 3) == 3) {   // bring the larger of the two minors into [1, 2)
+          const float mx = fmaxf(fabsf(P), fabsf(Pp));
+          const float f = __int_as_float((254 - ((__float_as_int(mx) >> 23) & 0xFF)) << 23);
+          P *= f;
+          Pp *= f;
+        }
+      }
+      // eigenvalue i lies in (x_t, x_t+1] where cnt(x_t) <= i < cnt(x_t+1)
+      float lo = cnt <= i ? x : a, hi = cnt > i ? x : b;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        lo = fmaxf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fminf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      a = lo;
+      b = hi;
+    }
+    if (t == 0) S.tri_lam[i] = 0.5f * (a + b);
+  }
+  __syncthreads();
+  // ---- inverse iteration (warp 0, lane i < 16: eigenvalue i) on the scaled
+  // T: one factorisation of T - lambda I (no pivoting, pivots kept away from
+  // zero), two solves from distinct start vectors, then Gram-Schmidt inside
+  // clusters of close eigenvalues and the reflections back
+  if (warp == 0) {
+    const int i = lane & 15;
+    const float sc = S.tri_s[0];
+    float d[kPage], e[kPage];
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) {
+      d[j] = S.tri_d[j] * sc;
+      e[j] = S.tri_e[j] * sc;
+    }
+    const float lam = S.tri_lam[i];
+    const float tnorm = fmaxf(fabsf(S.tri_s[1]), fabsf(S.tri_s[2]));
+    const float floor_p = 1e-7f * tnorm;
+    float inv[kPage], cp[kPage];
+    {
+      float m = d[0] - lam;
+#pragma unroll
+      for (int j = 0; j < kPage; ++j) {
+        if (j > 0) m = fmaf(-e[j - 1], cp[j - 1], d[j] - lam);
+        if (fabsf(m) < floor_p) m = m < 0.f ? -floor_p : floor_p;
+        inv[j] = fast_rcp(m);
+        cp[j] = e[j] * inv[j];
+      }
+    }
+    float x[kPage];
+#pragma unroll
+    for (int j = 0; j < kPage; ++j) x[j] = fmaf((float)(((j + 1) * (i + 3) * 7) % 13), 0.37f / 13.f, 1.f);
+#pragma unroll 1
+    for (int it = 0; it < 2; ++it) {
+      float y = x[0] * inv[0];
+      x[0] = y;
+#pragma unroll
+      for (int j = 1; j < kPage; ++j) {
+        y = fmaf(-e[j - 1], y, x[j]) * inv[j];
+        x[j] = y;
+      }
+#pragma unroll
+      for (int j = kPage - 2; j >= 0; --j) x[j] = fmaf(-cp[j], x[j + 1], x[j]);
+      float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPage; j += 2) {
+        m0 = fmaxf(m0, fabsf(x[j]));
+        m1 = fmaxf(m1, fabsf(x[j + 1]));
+      }
+      const float mx = fmaxf(m0, m1);
+      const float s = mx > 0.f ? fast_rcp(mx) : 1.f;
+#pragma unroll
+      for (int j = 0; j < kPage; ++j) x[j] *= s;
+    }
+    {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPage; j += 2) {
+        s0 = fmaf(x[j], x[j], s0);
+        s1 = fmaf(x[j + 1], x[j + 1], s1);
+      }
+      const float rn = rsqrtf(fmaxf(s0 + s1, 1e-30f));
+#pragma unroll
+      for (int j = 0; j < kPage; ++j) x[j] *= rn;
+    }
+    // clusters: eigenvalue i joins i - 1's when closer than 1e-3 of |T|
+    const float ctol = 1e-3f * tnorm;
+    const bool joins = i > 0 && (lam - S.tri_lam[i - 1]) <= ctol;
+    if (__any_sync(0xffffffffu, lane < kPage && joins)) {
+      float* Yv = S.W[1];   // [16][16]: eigenvector i at row i
+      if (lane < kPage)
+#pragma unroll
+        for (int j = 0; j < kPage; ++j) Yv[i * kPage + j] = x[j];
+      __syncwarp();
+      // in index order, each member of a cluster is made orthogonal to the
+      // members before it, then normalised
+      for (int mbr = 1; mbr < kPage; ++mbr) {
+        if (lane == mbr && joins) {
+          int first = mbr;
+          while (first > 0 && S.tri_lam[first] - S.tri_lam[first - 1] <= ctol) --first;
+          for (int q = first; q < mbr; ++q) {
+            float dot = 0.f;
+#pragma unroll
+            for (int j = 0; j < kPage; ++j) dot = fmaf(Yv[q * kPage + j], x[j], dot);
+#pragma unroll
+            for (int j = 0; j < kPage; ++j) x[j] = fmaf(-dot, Yv[q * kPage + j], x[j]);
+          }
+          float ss = 0.f;
+#pragma unroll
+          for (int j = 0; j < kPage; ++j) ss = fmaf(x[j], x[j], ss);
+          const float rn = rsqrtf(fmaxf(ss, 1e-30f));
+#pragma unroll
+          for (int j = 0; j < kPage; ++j) {
+            x[j] *= rn;
+            Yv[i * kPage + j] = x[j];
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // back to the Gram matrix's basis: z = H_0 (H_1 (... (H_13 x))); v_k is
+    // zero at indices up to k, so the full-length products change nothing there
+#pragma unroll 1
+    for (int k = kPage - 3; k >= 0; --k) {
+      float hv[kPage];
+#pragma unroll
+      for (int j = 0; j < kPage; j += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(&HV[k * kPage + j]);
+        hv[j] = q.x;
+        hv[j + 1] = q.y;
+        hv[j + 2] = q.z;
+        hv[j + 3] = q.w;
+      }
+      float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPage; j += 2) {
+        t0 = fmaf(hv[j], x[j], t0);
+        t1 = fmaf(hv[j + 1], x[j + 1], t1);
+      }
+      const float m2 = -2.f * (t0 + t1);
+#pragma unroll
+      for (int j = 0; j < kPage; ++j) x[j] = fmaf(m2, hv[j], x[j]);
+    }
+    if (lane < kPage) {
+#pragma unroll
+      for (int j = 0; j < kPage; ++j) S.W[0][j * kPage + i] = x[j];
+      S.G[0][i * kPage + i] = S.tri_s[3] > 1e-30f ? lam / sc : 0.f;   // a zero matrix: every eigenvalue 0
+    }
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParams p) {
   __shared__ PageSmem S;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Jacobi roles
-  const bool rot = warp == 0;                                      // lanes j and j + 16 agree; j stores
-  const int j = lane & 15;
-  const bool gblk = warp == 1 || warp == 2;
-  const bool wblk = warp == 3 || warp >= 5;
-  const int gb = (warp - 1) * 32 + lane;                          // G block: row pair gb / 8, column pair gb % 8
-  const int wb = (warp == 3 ? 0 : warp - 4) * 32 + lane;          // W: row wb / 8, column pair wb % 8
   griddep_launch_dependents();
   int64_t blk;
   int h;
   if (!target_of(p, blockIdx.x, tid == 0, blk, h)) return;   // uniform over the CTA
 
-  // ---- 1. keys (key row t / 16, dims 8 (t % 16) ..), the round schedule
-  // tabled while they arrive, centroid, centred keys
+  // ---- 1. keys (key row t / 16, dims 8 (t % 16) ..), centroid, centred keys
   const int kr = tid >> 4, kc = tid & 15;
   const uint4 raw = *reinterpret_cast<const uint4*>(p.k_cache + (blk * p.H_kv + h) * (int64_t)(kPage * kHeadDim) +
                                                     kr * kHeadDim + 8 * kc);
-  if (tid < 15 * 8) {
-    const int R = tid >> 3, k = tid & 7;
-    int seen = 0, lo = 0;
-    for (int i = 0; i < kPage; ++i) {
-      const bool first = i < jacobi_partner(i, R);
-      if (first && seen == k) lo = i;
-      seen += first;
-    }
-    S.pairs[R][k] = (uint16_t)(lo | jacobi_partner(lo, R) << 8);
-  } else if (tid >= 128) {
-    for (int x = tid - 128; x < 15 * kPage; x += kPbThreads - 128) {
-      const int R = x >> 4, jx = x & 15;
-      const int q = jacobi_partner(jx, R == 14 ? 0 : R + 1);
-      const int lo = min(jx, q), hi = max(jx, q);
-      const int plo = jacobi_partner(lo, R), phi = jacobi_partner(hi, R);
-      S.sched_p[R][jx] = make_uint4(pack4(lo * 16 + lo, plo * 16 + lo, lo * 16 + plo, plo * 16 + plo),
-                                   pack4(hi * 16 + hi, phi * 16 + hi, hi * 16 + phi, phi * 16 + phi),
-                                   pack4(lo * 16 + hi, plo * 16 + hi, lo * 16 + phi, plo * 16 + phi),
-                                   (uint32_t)lo | (uint32_t)hi << 8);
-    }
-  }
   {
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
     float* xr = &S.X[kr * kXStride + 8 * kc];
@@ -537,147 +794,26 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
   for (int e = 0; e < 8; ++e) S.X[kr * kXStride + 8 * kc + e] -= S.mu[8 * kc + e];
   __syncthreads();
 
-  // ---- 2. Gram entry (kr, kc), W = I
+  // ---- 2. Gram entry (kr, kc): four partial sums, each the same for (kc, kr),
+  // so G is symmetric bit for bit (the reduction relies on it)
   {
-    float g = 0.f;
+    float g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f;
+#pragma unroll 8
     for (int d = 0; d < kHeadDim; d += 4) {
       const float4 xi = *reinterpret_cast<const float4*>(&S.X[kr * kXStride + d]);
       const float4 xj = *reinterpret_cast<const float4*>(&S.X[kc * kXStride + d]);
-      g = fmaf(xi.x, xj.x, g);
-      g = fmaf(xi.y, xj.y, g);
-      g = fmaf(xi.z, xj.z, g);
-      g = fmaf(xi.w, xj.w, g);
+      g0 = fmaf(xi.x, xj.x, g0);
+      g1 = fmaf(xi.y, xj.y, g1);
+      g2 = fmaf(xi.z, xj.z, g2);
+      g3 = fmaf(xi.w, xj.w, g3);
     }
-    S.G[0][tid] = g;
-    S.W[0][tid] = kr == kc ? 1.f : 0.f;
+    S.G[0][tid] = (g0 + g1) + (g2 + g3);
   }
   __syncthreads();
-  // round 0's rotations, from the Gram matrix; lane j keeps (c, signed s)
-  // of index j's pair in my_cs for the next round's pivots
-  float2 my_cs = make_float2(1.f, 0.f);
-  if (rot) {
-    const int q = jacobi_partner(j, 0);
-    const int lo = min(j, q), hi = max(j, q);
-    const float2 cs = jacobi_cs(S.G[0][lo * kPage + lo], S.G[0][hi * kPage + hi], S.G[0][lo * kPage + hi]);
-    my_cs = make_float2(cs.x, j == lo ? -cs.y : cs.y);
-    if (lane < kPage) S.cs[0][j] = my_cs;
-  }
-  __syncthreads();
-
-  // ---- 3. Jacobi: kSweeps sweeps of 15 rounds, with no CTA-wide barrier in
-  // the loop.  Named barriers pass each hand-off:
-  //   1 (rotation warp waits; G and W warps arrive): round R's blocks have
-  //     stored G and W and read the round's (c, s);
-  //   4 (rotation warp arrives; G and W warps wait): the next round's (c, s)
-  //     are stored; the rotation warp releases them only after barrier 1, so
-  //     no warp can arrive at 1 for a round before 1 has completed the last;
-  //   2 (G warps) and 3 (W warps): a group's stores of a round are complete,
-  //     so it can load its operands of the next round before barrier 4.
-  // The rotation warp keeps its own lanes' rotations and loads the G entries
-  // of its next pivots once barrier 1 has passed.
-  uint4 op = rot ? S.sched_p[0][j] : make_uint4(0, 0, 0, 0);
-  float gv[12];   // rotation lanes: G at the 12 operand positions of this round's pivots
-                  // G blocks: gv[0..3] = the block; W: gv[0..1] = the row's pair
-  int pr = 0, pc = 0;   // this round's row / column pair of the block (lo | hi << 8)
-#pragma unroll
-  for (int q = 0; q < 12; ++q) gv[q] = 0.f;
-  if (rot) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      gv[q] = S.G[0][(op.x >> (8 * q)) & 0xFF];
-      gv[4 + q] = S.G[0][(op.y >> (8 * q)) & 0xFF];
-      gv[8 + q] = S.G[0][(op.z >> (8 * q)) & 0xFF];
-    }
-  } else if (gblk) {
-    pr = S.pairs[0][gb >> 3];
-    pc = S.pairs[0][gb & 7];
-    const int r = pr & 0xFF, rp = pr >> 8, c = pc & 0xFF, cq = pc >> 8;
-    gv[0] = S.G[0][r * kPage + c];
-    gv[1] = S.G[0][r * kPage + cq];
-    gv[2] = S.G[0][rp * kPage + c];
-    gv[3] = S.G[0][rp * kPage + cq];
-  } else if (wblk) {
-    pc = S.pairs[0][wb & 7];
-    gv[0] = S.W[0][(wb >> 3) * kPage + (pc & 0xFF)];
-    gv[1] = S.W[0][(wb >> 3) * kPage + (pc >> 8)];
-  }
-  if (rot) {
-    for (int it = 0, R = 0; it < kPbRounds; ++it) {
-      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
-      // the next round's pivots from this round's rotations, then its rotation
-      // j is lo or hi: the other index's rotation comes from its lane
-      const int lo = op.w & 0xFF, hi = (op.w >> 8) & 0xFF;
-      const float2 other = make_float2(__shfl_sync(0xffffffffu, my_cs.x, lo + hi - j),
-                                       __shfl_sync(0xffffffffu, my_cs.y, lo + hi - j));
-      const float2 clo = j == lo ? my_cs : other, chi = j == lo ? other : my_cs;
-      auto entry = [&](const float* v, float2 cx, float2 cy) {
-        return rot_signed(cy.x, cy.y, rot_signed(cx.x, cx.y, v[0], v[1]), rot_signed(cx.x, cx.y, v[2], v[3]));
-      };
-      const float a = entry(gv, clo, clo);
-      const float bb = entry(gv + 4, chi, chi);
-      const float e = entry(gv + 8, clo, chi);
-      op = S.sched_p[Rn][j];
-      const float2 rt = jacobi_cs(a, bb, e);
-      my_cs = make_float2(rt.x, j == lo ? -rt.y : rt.y);
-      // (the buffer's previous round was read before barrier 1 of the last round)
-      if (lane < kPage) S.cs[cur ^ 1][j] = my_cs;
-      asm volatile("bar.sync 1, 224;" ::: "memory");   // round R's blocks are done
-      if (it + 1 < kPbRounds) asm volatile("bar.arrive 4, 224;" ::: "memory");
-      const float* Gn = S.G[cur ^ 1];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        gv[q] = Gn[(op.x >> (8 * q)) & 0xFF];
-        gv[4 + q] = Gn[(op.y >> (8 * q)) & 0xFF];
-        gv[8 + q] = Gn[(op.z >> (8 * q)) & 0xFF];
-      }
-      R = Rn;
-    }
-  } else if (gblk) {
-    for (int it = 0, R = 0; it < kPbRounds; ++it) {
-      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
-      if (it > 0) asm volatile("bar.sync 4, 224;" ::: "memory");   // this round's (c, s)
-      // block rows (r, rp) x columns (c, cp): rows rotated, then columns;
-      // index rp's signed s is the negation of index r's
-      const int r = pr & 0xFF, rp = pr >> 8, c = pc & 0xFF, cq = pc >> 8;
-      const float2 cr = S.cs[cur][r], cc = S.cs[cur][c];
-      const float a00 = rot_signed(cr.x, cr.y, gv[0], gv[2]), a01 = rot_signed(cr.x, cr.y, gv[1], gv[3]);
-      const float a10 = rot_signed(cr.x, -cr.y, gv[2], gv[0]), a11 = rot_signed(cr.x, -cr.y, gv[3], gv[1]);
-      float* Gn = S.G[cur ^ 1];
-      Gn[r * kPage + c] = rot_signed(cc.x, cc.y, a00, a01);
-      Gn[r * kPage + cq] = rot_signed(cc.x, -cc.y, a01, a00);
-      Gn[rp * kPage + c] = rot_signed(cc.x, cc.y, a10, a11);
-      Gn[rp * kPage + cq] = rot_signed(cc.x, -cc.y, a11, a10);
-      asm volatile("bar.arrive 1, 224;" ::: "memory");
-      pr = S.pairs[Rn][gb >> 3];
-      pc = S.pairs[Rn][gb & 7];
-      asm volatile("bar.sync 2, 64;" ::: "memory");
-      const int r2 = pr & 0xFF, rp2 = pr >> 8, c2 = pc & 0xFF, cq2 = pc >> 8;
-      gv[0] = Gn[r2 * kPage + c2];
-      gv[1] = Gn[r2 * kPage + cq2];
-      gv[2] = Gn[rp2 * kPage + c2];
-      gv[3] = Gn[rp2 * kPage + cq2];
-      R = Rn;
-    }
-  } else if (wblk) {
-    for (int it = 0, R = 0; it < kPbRounds; ++it) {
-      const int cur = it & 1, Rn = R == 14 ? 0 : R + 1;
-      if (it > 0) asm volatile("bar.sync 4, 224;" ::: "memory");
-      const int row = wb >> 3, c = pc & 0xFF, cq = pc >> 8;
-      const float2 cc = S.cs[cur][c];
-      float* Wn = S.W[cur ^ 1];
-      Wn[row * kPage + c] = rot_signed(cc.x, cc.y, gv[0], gv[1]);
-      Wn[row * kPage + cq] = rot_signed(cc.x, -cc.y, gv[1], gv[0]);
-      asm volatile("bar.arrive 1, 224;" ::: "memory");
-      pc = S.pairs[Rn][wb & 7];
-      asm volatile("bar.sync 3, 128;" ::: "memory");
-      gv[0] = Wn[row * kPage + (pc & 0xFF)];
-      gv[1] = Wn[row * kPage + (pc >> 8)];
-      R = Rn;
-    }
-  }
-  __syncthreads();
-  const float* Gf = S.G[kPbRounds & 1];
-  const float* Wf = S.W[kPbRounds & 1];
+  // ---- 3. eigenpairs: eigenvalue i at G[i][i], its vector in column i of W
+  page_eigen_tridiag(S, tid);
+  const float* Gf = S.G[0];
+  const float* Wf = S.W[0];
 
   // ---- 4. rank the eigenvalues, top r, signs (warp 0; lanes 16..31 mirror 0..15)
   if (warp == 0) {

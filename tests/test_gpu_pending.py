@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from sparse_long_context_locks_gb300 import locks as L
 from sparse_long_context_locks_gb300 import workload as W
 
@@ -21,7 +22,7 @@ def _w(**kw):
     return W.Workload(**base)
 
 
-def test_build_pending_matches_build_and_reads_the_device_count():
+def test_build_pending_reads_the_device_count():
     w = _w(batch=3, context=16 * 60, context_hi=16 * 120)
     d = W.generate(w, device="cuda")
     H = w.num_kv_heads
@@ -45,7 +46,8 @@ def test_build_pending_matches_build_and_reads_the_device_count():
         g.replay()
         torch.cuda.synchronize()
         built = pick[:k].long()
-        assert torch.equal(summ[built], ref[built])
+        for h in range(H):   # against the oracle's decomposition of the same keys
+            check_records(summ[built, h].cpu().numpy(), d["k_cache"][built, h].double().cpu().numpy())
         rest = torch.ones(d["num_blocks"], dtype=torch.bool, device="cuda")
         rest[built] = False
         assert int(summ[rest].count_nonzero()) == 0
@@ -146,9 +148,10 @@ def test_decode_step_crossing_in_a_graph_replays():
     H = w.num_kv_heads
     summ = torch.zeros(d["num_blocks"], H, 784, dtype=torch.uint8, device="cuda")
     L.locks_build_summaries(H, d["k_cache"], W.full_page_blocks(d).cuda(), summ)
-    ref = summ.clone()
+    bulk = summ.clone()
     last = [int(d["block_table"][b, int(d["seq_lens"][b]) // 16 - 1]) for b in range(2)]
-    summ[torch.tensor(last).long()] = 0
+    new = torch.tensor(last).long()
+    summ[new] = 0
     bufs = L.DecodeBuffers(H, w.batch, w.max_pages, w.budget_pages)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -156,14 +159,20 @@ def test_decode_step_crossing_in_a_graph_replays():
                                      d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected, bufs.out,
                                      bufs.workspace, scores=bufs.scores, stream=s)
         s.synchronize()
+        ref = summ.clone()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             L.locks_decode_step_crossing(H, d["q"], summ, d["k_cache"], d["v_cache"], d["block_table"],
                                          d["seq_lens"], w.budget_pages, bufs.selected, bufs.n_selected,
                                          bufs.out, bufs.workspace, scores=bufs.scores, stream=s)
     first = bufs.out.clone()
+    rest = torch.ones(d["num_blocks"], dtype=torch.bool, device="cuda")
+    rest[new] = False
+    assert torch.equal(ref[rest], bulk[rest])                  # only the new pages were written
+    for h in range(H):
+        check_records(ref[new, h].cpu().numpy(), d["k_cache"][new, h].double().cpu().numpy())
     for _ in range(3):
-        summ[torch.tensor(last).long()] = 0
+        summ[new] = 0
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(summ, ref)
@@ -171,10 +180,14 @@ def test_decode_step_crossing_in_a_graph_replays():
     assert L.locks_read_status(bufs.workspace) == 0
 
 
-def test_build_pending_special_pages_equal_the_bulk_build():
-    """The few-page builder (one CTA a page-head) must write the bulk
-    builder's records bit for bit: equal keys, exact low rank, a zero page,
-    large and tiny magnitudes, repeated eigenvalues, and random pages."""
+def test_build_pending_special_pages_against_the_oracle():
+    """Both builders on pages where an eigensolver can go wrong: equal keys,
+    exact low rank, a zero page, large and tiny magnitudes, 16 equal and two
+    repeated eigenvalues, a large centroid, and random pages.  The page
+    builder (Householder, multisection, inverse iteration) and the bulk
+    builder (Jacobi) each meet the oracle's records, and on the pages whose
+    top directions are unique their codes differ by at most one (a value on
+    a rounding edge)."""
     rng = np.random.default_rng(12)
     pages = [np.tile(rng.normal(size=128), (16, 1)),
              rng.integers(-3, 4, 128) + rng.integers(-3, 4, (16, 3)) @ rng.integers(-2, 3, (128, 3)).T,
@@ -188,17 +201,28 @@ def test_build_pending_special_pages_equal_the_bulk_build():
     for s in (0.05, 1.0, 30.0):
         pages += [rng.normal(size=(16, 128)) * s for _ in range(8)]
     K = torch.tensor(np.stack(pages), dtype=torch.bfloat16)              # 32 pages
+    Kd = K.double().numpy()
+    lam = O.page_summary(Kd)["lam"]
+    gaps = -np.diff(lam[:, :9], axis=1) / np.maximum(lam[:, :1], 1e-30)
+    unique = np.all(gaps > 1e-3, axis=1) & (lam[:, 7] > 1e-3 * lam[:, 0])
+    assert unique.sum() >= 24
     for H in (1, 2):
         kc = K.view(-1, H, 16, 128).contiguous().cuda()
         nblk = kc.shape[0]
         ids = torch.arange(nblk, dtype=torch.int32, device="cuda")
-        ref = torch.zeros(nblk, H, 784, dtype=torch.uint8, device="cuda")
-        got = torch.zeros_like(ref)
+        bulk = torch.zeros(nblk, H, 784, dtype=torch.uint8, device="cuda")
+        got = torch.zeros_like(bulk)
         ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-        L.locks_build_summaries(H, kc, ids, ref, ws)
+        L.locks_build_summaries(H, kc, ids, bulk, ws)
         n = torch.full((1,), nblk, dtype=torch.int32, device="cuda")
         L.locks_build_pending(H, kc, ids, n, got, ws)
         torch.cuda.synchronize()
         assert L.locks_read_status(ws) == 0
-        diff = (got != ref).any(dim=-1).nonzero().tolist()
-        assert not diff, f"H={H}: records differ at (block, head) {diff[:8]}"
+        for rec in (got, bulk):
+            check_records(rec.view(-1, 784).cpu().numpy(), Kd)
+        g = O.decode_records(got.view(-1, 784).cpu().numpy())
+        b = O.decode_records(bulk.view(-1, 784).cpu().numpy())
+        assert np.array_equal(g["muq"], b["muq"])
+        for key in ("Vq", "Cq"):
+            diff = np.abs(g[key].astype(np.int64) - b[key].astype(np.int64))[unique]
+            assert diff.max() <= 1, key
