@@ -11,8 +11,15 @@ once into a CUDA graph and replayed.
                   [--workload llama8b_128k] [--extra-workloads ctx1m,batch16_32k]
 
 Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
-events on the launching stream; between timed steps L2 is flushed by reading a
-256 MB buffer (the step's inputs are smaller than L2), outside the events.
+events on the launching stream.  The timed steps rotate over copies of the
+layer's K/V cache and records (32 at 128K: 1.9 GB), as the layers of a decode
+pass do, so the inputs are larger than L2 and each step reads its K/V and
+records from HBM while the kernels' code stays cached; where the copies do not
+fit, L2 is flushed before each step by reading a 256 MB buffer instead (the
+line's config.l2 says which).  The per-kernel rows time one graph replay each
+with L2 flushed before it, code included (rows.step_us: the whole step timed
+that way, the comparator's ratios taken on it; rows.step_us_rotated: the
+headline's step).
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling),
 the per-rank times are max-reduced and rank 0 prints one JSON line.
 
@@ -530,11 +537,42 @@ def main():
     case = WorkloadCase(L, w, data, summ, bufs, capture)
     g_step = case.g_step
 
-    # ---------------------------------------------------------------- timed steps
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
+    # ---------------------------------------------------------------- rotation
+    # The timed steps rotate over copies of the layer's K/V cache and records,
+    # as the layers of a decode pass do (the content repeats, the memory does
+    # not; q, the block table and the lengths are shared as in a paged
+    # engine).  The copies' inputs exceed L2 several times over, so every
+    # step's K/V and records come from HBM while the kernels' code stays
+    # cached.  Where the copies do not fit, the steps run on the one copy with
+    # L2 flushed before each.
+    layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
+    n_copies = max(32 if layer_bytes <= (64 << 20) else 2, -(-4 * l2_bytes // by_step(w, data)))
+    kv, g_rot = [], []
+    if torch.cuda.mem_get_info()[0] > n_copies * layer_bytes + (8 << 30):
+        kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_copies)]
+        for kc, vc, sm in kv:
+            g_rot.append(capture(lambda s, kc=kc, vc=vc, sm=sm: L.locks_decode_step(
+                H, data["q"], sm, kc, vc, data["block_table"], data["seq_lens"], w.budget_pages, bufs.selected,
+                bufs.n_selected, bufs.out, bufs.workspace, scores=bufs.scores, stream=s)))
+        config["l2"] = (f"inputs larger than L2: the timed steps rotate over {n_copies} copies of the layer's K/V "
+                        f"cache and records ({n_copies * layer_bytes / 1e9:.1f} GB), no flush; the flushed "
+                        f"single-step time is rows.step_us")
+        config["clocks_window"] = ("nvidia-smi every 100 ms over a >= 0.6 s lead-in of the same rotation "
+                                   "and the timed steps")
+
+    def timed_step(i):
+        """Step i of the timed (or lead-in) loop: the next copy, else a flush and the one copy."""
+        if g_rot:
+            g_rot[i % len(g_rot)].replay()
+        else:
             flush_l2()
             g_step.replay()
+
+    # ---------------------------------------------------------------- timed steps
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup, len(g_rot))):
+            timed_step(i)
     stream.synchronize()
     sampler = ClockSampler(local)
     K = args.steps
@@ -547,9 +585,8 @@ def main():
     t_lead = time.perf_counter()
     with torch.cuda.stream(stream):
         while True:
-            for _ in range(64):
-                flush_l2()
-                g_step.replay()
+            for i in range(64):
+                timed_step(i)
             stream.synchronize()
             el = time.perf_counter() - t_lead
             if sampler.proc is None or el > 10.0 or (el > 0.6 and sampler.count() >= 4):
@@ -561,9 +598,13 @@ def main():
     torch.cuda.nvtx.range_push("timed_steps")   # ncu --nvtx-include "timed_steps/" selects these launches
     with torch.cuda.stream(stream):
         for i in range(K):
-            flush_l2()
-            ev[i][0].record(stream)
-            g_step.replay()
+            if g_rot:
+                ev[i][0].record(stream)
+                g_rot[i % len(g_rot)].replay()
+            else:
+                flush_l2()
+                ev[i][0].record(stream)
+                g_step.replay()
             ev[i][1].record(stream)
     stream.synchronize()
     torch.cuda.nvtx.range_pop()
@@ -584,7 +625,15 @@ def main():
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
 
     # ---------------------------------------------------------------- per-kernel rows
-    main_rows, kernels = case.measure(time_graph, peak, n_sms, step_us=ms_step * 1e3)
+    # rows.step_us is the single step with L2 flushed before it, like every
+    # other row (the dense comparator's included, so the ratios compare like
+    # with like); the headline's own time is rows.step_us_rotated
+    main_rows, kernels = case.measure(time_graph, peak, n_sms, step_us=None if g_rot else ms_step * 1e3)
+    main_rows["step_us_rotated"] = ms_step * 1e3 if g_rot else None
+    main_rows["step_timing"] = config["l2"]
+    head_gbs = by_step(w, data) / (ms_step * 1e-3) / 1e9
+    roofline_step = {"achieved": head_gbs, "peak": peak, "unit": "GB/s", "frac": head_gbs / peak,
+                     "algorithmic_bytes": by_step(w, data), "step": "the headline's timed steps"}
     launches_per_step = len(kernels)
     dominant = max(kernels, key=lambda k: k["us"])
     roofline = dict(dominant, peak_source=peak_src)
@@ -640,7 +689,6 @@ def main():
     # data comes from HBM while the kernels' code stays cached, as in real
     # decoding.
     n_layers = 32
-    layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
     # the selection of one step on the workload's own lengths (the rows above
     # left the crossing lengths' selection in the buffers)
     with torch.cuda.stream(stream):
@@ -650,11 +698,12 @@ def main():
     stream.synchronize()
     quality = selection_quality(w, data, bufs.selected, bufs.n_selected) if rank == 0 else None
     layers32 = None
-    if args.layers32 and torch.cuda.mem_get_info()[0] > n_layers * layer_bytes + (8 << 30):
-        kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_layers)]
+    if args.layers32 and (len(kv) >= n_layers or torch.cuda.mem_get_info()[0] > n_layers * layer_bytes + (8 << 30)):
+        if len(kv) < n_layers:
+            kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_layers)]
 
         def pass32(s):
-            for kc, vc, sm in kv:
+            for kc, vc, sm in kv[:n_layers]:
                 L.locks_decode_step(H, data["q"], sm, kc, vc, data["block_table"], data["seq_lens"],
                                     w.budget_pages, bufs.selected, bufs.n_selected, bufs.out, bufs.workspace,
                                     scores=bufs.scores, stream=s)
@@ -676,8 +725,10 @@ def main():
                     "mode": "32 locks_decode_step calls over 32 distinct copies of the layer's K/V and records "
                             "in one graph, replayed back to back with no L2 flush (1.9 GB of inputs a pass)"}
         layers32["frac"] = layers32["GBps"] / peak
-        del kv, g32
-        torch.cuda.empty_cache()
+        del g32
+    g_rot.clear()      # the rotation's graphs read the copies: drop them first
+    kv = []
+    torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- e2e
     # the step's per-token inputs (q and the sequence lengths) packed in one
@@ -787,7 +838,7 @@ def main():
         "gpu_launches": launches_per_step * K,
         "roofline": roofline,
         "roofline_kernels": kernels,
-        "roofline_step": main_rows["roofline_step"],
+        "roofline_step": roofline_step,
         "quality": quality,
         "rows": main_rows,
         "layers32": layers32,
