@@ -218,6 +218,12 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // ---------------------------------------------------------------- conversions
+// The conversions below use the known "magic number" method: a bitwise op
+// places the integer under a fixed f16 exponent and one subtraction removes
+// the exponent's value (for int4/int8 -> f16 with LOP3 see Kim et al., "Who
+// Says Elephants Can't Run: Bringing Large Scale MoE Models into Cloud Scale
+// Production", 2022).  The variants here are exact for two's-complement
+// codes.
 // (a & b) ^ c in one LOP3.
 __device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
