@@ -106,8 +106,8 @@ def parse():
     ap.add_argument("--no-layers32", dest="layers32", action="store_false",
                     help="skip the 32-layer pass row")
     ap.add_argument("--profile-run", action="store_true",
-                    help="warm-up and timed steps only (no per-kernel rows, e2e or CPU baseline): "
-                         "the command the ncu captures run")
+                    help="warm-up and timed steps only (no per-kernel rows, e2e or CPU baseline; one copy "
+                         "of the inputs, L2 flushed before each step): the command the ncu captures run")
     return ap.parse_args()
 
 
@@ -549,7 +549,9 @@ def main():
     l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
     n_copies = max(32 if layer_bytes <= (64 << 20) else 2, -(-4 * l2_bytes // by_step(w, data)))
     kv, g_rot = [], []
-    if torch.cuda.mem_get_info()[0] > n_copies * layer_bytes + (8 << 30):
+    # (a profile run keeps one copy and the flush: ncu saves and restores the
+    # device memory around its passes, so the copies would only slow it)
+    if not args.profile_run and torch.cuda.mem_get_info()[0] > n_copies * layer_bytes + (8 << 30):
         kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_copies)]
         for kc, vc, sm in kv:
             g_rot.append(capture(lambda s, kc=kc, vc=vc, sm=sm: L.locks_decode_step(
