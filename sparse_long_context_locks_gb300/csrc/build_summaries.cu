@@ -501,6 +501,8 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
       const float x0 = xs[1];
       float alpha = x0, v0 = 0.f, inv = 0.f;
       if (sig > 0.f) {
+        // correctly rounded: the entries the reflection zeroes are dropped, not
+        // formed, so an ulp of error here lands on the small eigenvalues
         const float nrm = sqrtf(fmaf(x0, x0, sig));
         alpha = x0 >= 0.f ? -nrm : nrm;
         v0 = x0 - alpha;
@@ -518,36 +520,37 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
         S.tri_d[k] = xs[0];
         S.tri_e[k] = alpha;
       }
-      // p = A v (row l of A is column l), then w = 2 p - 2 (v.p) v
+      // 2p = 2 A v (row l of A is column l), then w = 2p - 2 (v.p) v
       float p0 = 0.f, p1 = 0.f;
 #pragma unroll
       for (int i = 1; i < kPage; ++i) {
         if (i & 1) p1 = fmaf(a[i], v[i], p1);
         else p0 = fmaf(a[i], v[i], p0);
       }
-      const float pl = p0 + p1;
-      float pv[kPage];
+      const float pl2 = 2.f * (p0 + p1);
+      float pv2[kPage];
 #pragma unroll
       for (int i = 1; i < kPage; ++i) {
-        const float t = __shfl_sync(0xffffffffu, pl, k + i);
-        pv[i] = k + i < kPage ? t : 0.f;
+        const float t = __shfl_sync(0xffffffffu, pl2, k + i);
+        pv2[i] = k + i < kPage ? t : 0.f;
       }
       float K0 = 0.f, K1 = 0.f;
 #pragma unroll
       for (int i = 1; i < kPage; ++i) {
-        if (i & 1) K1 = fmaf(v[i], pv[i], K1);
-        else K0 = fmaf(v[i], pv[i], K0);
+        if (i & 1) K1 = fmaf(v[i], pv2[i], K1);
+        else K0 = fmaf(v[i], pv2[i], K0);
       }
-      const float m2K = -2.f * (K0 + K1);
-      const float wl = fmaf(m2K, vl, 2.f * pl);
+      const float m2K = -(K0 + K1);   // -2 (v.p)
+      const float wl = fmaf(m2K, vl, pl2);
       // A -= v w^T + w v^T on rows and columns past k: both products are
-      // rounded, then added, so elements (i, l) and (l, i) stay equal; row
-      // and column k are final (d_k, e_k) and drop out
+      // rounded, then added, so elements (i, l) and (l, i) stay equal (a
+      // fused form drifts apart by an ulp a step, and the reflectors built
+      // from one side then amplify it).  Lanes up to k hold columns no later
+      // step reads; row and column k are final (d_k, e_k) and drop out.
 #pragma unroll
       for (int i = 1; i < kPage; ++i) {
-        const float wi = fmaf(m2K, v[i], 2.f * pv[i]);
-        const float upd = __fadd_rn(__fmul_rn(v[i], wl), __fmul_rn(wi, vl));
-        a[i - 1] = l > k ? __fsub_rn(a[i], upd) : a[i];
+        const float wi = fmaf(m2K, v[i], pv2[i]);
+        a[i - 1] = __fsub_rn(a[i], __fadd_rn(__fmul_rn(v[i], wl), __fmul_rn(wi, vl)));
       }
       a[kPage - 1] = 0.f;
     }
@@ -587,12 +590,15 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
   {
     const int i = tid >> 4, t = tid & 15;
     const float sc = S.tri_s[0];
-    float d[kPage], me2[kPage];   // scaled diagonal, minus the scaled squared subdiagonal
+    // scaled diagonal, minus the scaled squared subdiagonal floored at 2^-60
+    // (eigenvalues move by at most 2^-30 of |T|): a zero minor is then never
+    // followed by another
+    float d[kPage], me2[kPage];
 #pragma unroll
     for (int j = 0; j < kPage; ++j) {
       d[j] = S.tri_d[j] * sc;
       const float ej = S.tri_e[j] * sc;
-      me2[j] = -ej * ej;
+      me2[j] = -fmaxf(ej * ej, 0x1p-60f);
     }
     float a = S.tri_s[1], b = S.tri_s[2];
 #pragma unroll 1
@@ -600,15 +606,14 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
       const float x = fmaf((b - a) * (1.f / 17.f), (float)(t + 1), a);
       // leading minors P_j of T - x I: P_0 = 1, P_1 = d_0 - x,
       // P_{j+1} = (d_j - x) P_j - e_{j-1}^2 P_{j-1}; a sign change from P_j
-      // to P_{j+1} is a negative pivot, one eigenvalue below x.  An exact
-      // zero takes the sign opposite to its predecessor's (a pivot of -0).
+      // to P_{j+1} is a negative pivot, one eigenvalue below x.  A zero minor
+      // counts as positive: its successor -e^2 P_{j-1} then carries the one
+      // change of the pair, as a pivot of -0 would have.
       float Pp = 1.f, P = d[0] - x;
-      if (P == 0.f) P = -0x1p-120f;
       int cnt = P < 0.f;
 #pragma unroll
       for (int j = 1; j < kPage; ++j) {
-        float Pn = fmaf(d[j] - x, P, me2[j - 1] * Pp);
-        if (Pn == 0.f) Pn = P < 0.f ? 0x1p-120f : -0x1p-120f;
+        const float Pn = fmaf(d[j] - x, P, me2[j - 1] * Pp);
         cnt += (Pn < 0.f) != (P < 0.f);
         Pp = P;
         P = Pn;
