@@ -700,9 +700,13 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
 #pragma unroll
       for (int j = 0; j < kPage; ++j) x[j] *= rn;
     }
-    // clusters: eigenvalue i joins i - 1's when closer than 1e-3 of |T|
+    // clusters among the top kRank eigenvalues (indices kRank .. 15, the only
+    // vectors the record keeps; the ranking below breaks ties toward the
+    // higher index): eigenvalue i joins i - 1's when closer than 1e-3 of |T|.
+    // The small eigenvalues of a nearly low-rank page form one wide cluster,
+    // whose serial orthogonalisation would buy nothing.
     const float ctol = 1e-3f * tnorm;
-    const bool joins = i > 0 && (lam - S.tri_lam[i - 1]) <= ctol;
+    const bool joins = i > kRank && (lam - S.tri_lam[i - 1]) <= ctol;
     if (__any_sync(0xffffffffu, lane < kPage && joins)) {
       float* Yv = S.W[1];   // [16][16]: eigenvector i at row i
       if (lane < kPage)
@@ -711,10 +715,10 @@ __device__ __forceinline__ void page_eigen_tridiag(PageSmem& S, int tid) {
       __syncwarp();
       // in index order, each member of a cluster is made orthogonal to the
       // members before it, then normalised
-      for (int mbr = 1; mbr < kPage; ++mbr) {
+      for (int mbr = kRank + 1; mbr < kPage; ++mbr) {
         if (lane == mbr && joins) {
           int first = mbr;
-          while (first > 0 && S.tri_lam[first] - S.tri_lam[first - 1] <= ctol) --first;
+          while (first > kRank && S.tri_lam[first] - S.tri_lam[first - 1] <= ctol) --first;
           for (int q = first; q < mbr; ++q) {
             float dot = 0.f;
 #pragma unroll
@@ -820,7 +824,10 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
   const float* Gf = S.G[0];
   const float* Wf = S.W[0];
 
-  // ---- 4. rank the eigenvalues, top r, signs (warp 0; lanes 16..31 mirror 0..15)
+  // ---- 4. rank the eigenvalues, top r, signs (warp 0; lanes 16..31 mirror
+  // 0..15).  The eigenvalues ascend with the index, and ties rank the higher
+  // index first, so the top r are indices 16 - r .. 15: the vectors that
+  // went through the clusters' orthogonalisation.
   if (warp == 0) {
     const int i = lane & 15;
     float lam[kPage];
@@ -835,7 +842,7 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
     float lam1 = lam[0];
 #pragma unroll
     for (int j = 0; j < kPage; ++j) {
-      pos += (lam[j] > my_lam) || (lam[j] == my_lam && j < i);
+      pos += (lam[j] > my_lam) || (lam[j] == my_lam && j > i);   // ties: higher index first
       lam1 = fmaxf(lam1, lam[j]);
     }
     if (lane < kPage) S.order[pos] = i;
