@@ -185,9 +185,12 @@ locks_status locks_build_summaries(const locks_cfg *cfg, const void *k_cache, in
                                    void *workspace, size_t workspace_bytes, locks_stream_t stream);
 
 /* Page-crossing build, §2 "page-local spectral decomposition" ("when a page
- * is finalised") and "implementation" (full CUDA graph): the same records as
- * locks_build_summaries for block_ids[0, min(*n_pending, max_pending)), where
- * n_pending points to a device int32 that the kernel reads.  One captured
+ * is finalised") and "implementation" (full CUDA graph): the records of
+ * block_ids[0, min(*n_pending, max_pending)), in the same format and to the
+ * same accuracy as locks_build_summaries (codes within one of the exact
+ * decomposition's; built for latency with a tridiagonal eigensolver, so not
+ * bit for bit the bulk builder's), where n_pending points to a device int32
+ * that the kernel reads.  One captured
  * graph thus serves every decode step, whatever number of requests crossed a
  * page boundary at that step (at most max_pending, e.g. one per request).
  * Entries at or past *n_pending are not read.  Launch it before
