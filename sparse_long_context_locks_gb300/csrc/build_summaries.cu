@@ -463,7 +463,9 @@ static_assert(offsetof(PageSmem, G) % 16 == 0 && (kPage * kPage * sizeof(float))
 // the classical alternative to Jacobi (Golub & Van Loan §8.3 for the
 // tridiagonal reduction and Sturm sequences, §8.2 for inverse iteration).
 // All kPbThreads threads call it.  On return S.G[0][i][i] holds eigenvalue i
-// (ascending in i) and column i of S.W[0] its unit eigenvector.
+// (ascending in i) and column i of S.W[0] its unit eigenvector; vectors of
+// close eigenvalues are orthogonalised only among i >= kRank, the ones the
+// record keeps.
 //
 // Built for latency, with three CTA barriers in all:
 //  * the reduction runs in warp 0's registers, lane l holding column l; the
