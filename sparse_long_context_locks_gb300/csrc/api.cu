@@ -434,7 +434,13 @@ locks_status score_impl(const locks_cfg* cfg, const void* q, const void* summari
   // (the fp32 scorer is launched in stream order: after the whole build)
   if (cfg->quant == 0) return from_cuda(launch_score_debug(p, cfg->rank, reinterpret_cast<cudaStream_t>(stream)));
   p.defer_crossing = defer_crossing ? 1 : 0;
-  return from_cuda(launch_score(p, pl.score_grid, reinterpret_cast<cudaStream_t>(stream), defer_crossing));
+  // In a crossing step each SM running a page-build CTA has room (registers)
+  // for one scorer CTA instead of two; the grid leaves those slots out
+  // (up to 16), so every scorer CTA starts at once instead of the last ones
+  // waiting for the build to end.
+  int grid = pl.score_grid;
+  if (defer_crossing) grid = max(1, min(grid, kTargetCtas - min(batch * cfg->num_kv_heads, 16)));
+  return from_cuda(launch_score(p, grid, reinterpret_cast<cudaStream_t>(stream), defer_crossing));
 }
 
 }  // namespace

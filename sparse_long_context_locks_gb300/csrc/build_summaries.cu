@@ -962,6 +962,14 @@ __global__ void __launch_bounds__(kPbThreads) build_page_kernel(const BuildParam
 cudaError_t launch_build_pages(const BuildParams& p, cudaStream_t stream) {
   const int64_t grid = (int64_t)p.n_build * p.H_kv;
   if (grid == 0) return cudaSuccess;
+  // The crossing step's scorer (98 KB of shared memory a CTA) shares SMs
+  // with these CTAs: with the default carveout an SM running one holds too
+  // little shared memory for any scorer CTA until it is idle again, and the
+  // scorer's last CTAs then start only when the build ends.
+  // (set on every call: the attribute belongs to the current device)
+  const cudaError_t carve = cudaFuncSetAttribute(build_page_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                 cudaSharedmemCarveoutMaxShared);
+  if (carve != cudaSuccess) return carve;
   build_page_kernel<<<(unsigned)grid, kPbThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
