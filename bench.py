@@ -452,12 +452,28 @@ def main():
     bufs = L.DecodeBuffers(H, B, w.max_pages, w.budget_pages)
     L.locks_build_summaries(H, data["k_cache"], blocks, summ, bufs.workspace)
     torch.cuda.synchronize()
+    # The timed steps rotate over copies of the layer's K/V cache and records,
+    # as the layers of a decode pass do (the content repeats, the memory does
+    # not; q, the block table and the lengths are shared as in a paged
+    # engine).  The copies' inputs exceed L2 several times over, so every
+    # step's K/V and records come from HBM while the kernels' code stays
+    # cached.  Where the copies do not fit (and in a profile run: ncu saves
+    # and restores the device memory around its passes), the steps run on the
+    # one copy with L2 flushed before each.  Decided here, so that the
+    # reference arm's config says the same.
+    layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
+    n_copies = max(32 if layer_bytes <= (64 << 20) else 2, -(-4 * l2_bytes // by_step(w, data)))
+    rotate = not args.profile_run and torch.cuda.mem_get_info()[0] > n_copies * layer_bytes + (8 << 30)
     config = {"workload": w.name, "batch": B, "context": w.context, "q_heads": H * G,
               "kv_heads": H, "head_dim": 128, "page": 16, "rank": 8,
               "budget_tokens": w.budget_tokens, "summary_bytes": 784,
-              "l2": "flushed between timed steps by reading a 256 MB buffer",
+              "l2": (f"inputs larger than L2: the timed steps rotate over {n_copies} copies of the layer's K/V "
+                     f"cache and records ({n_copies * layer_bytes / 1e9:.1f} GB), no flush; the flushed "
+                     f"single-step time is rows.step_us") if rotate else
+                    "flushed between timed steps by reading a 256 MB buffer",
               "clocks_window": "nvidia-smi every 100 ms over a >= 0.6 s lead-in of the same "
-                               "flush + step loop and the timed steps"}
+                               + ("rotation" if rotate else "flush + step loop") + " and the timed steps"}
 
     if args.impl == "reference":
         tmp = tempfile.mkdtemp(prefix="locks_oracle_")
@@ -538,30 +554,14 @@ def main():
     g_step = case.g_step
 
     # ---------------------------------------------------------------- rotation
-    # The timed steps rotate over copies of the layer's K/V cache and records,
-    # as the layers of a decode pass do (the content repeats, the memory does
-    # not; q, the block table and the lengths are shared as in a paged
-    # engine).  The copies' inputs exceed L2 several times over, so every
-    # step's K/V and records come from HBM while the kernels' code stays
-    # cached.  Where the copies do not fit, the steps run on the one copy with
-    # L2 flushed before each.
-    layer_bytes = 2 * data["k_cache"].numel() * 2 + summ.numel()
-    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
-    n_copies = max(32 if layer_bytes <= (64 << 20) else 2, -(-4 * l2_bytes // by_step(w, data)))
+    # (the copies and their graphs; see the config's "l2")
     kv, g_rot = [], []
-    # (a profile run keeps one copy and the flush: ncu saves and restores the
-    # device memory around its passes, so the copies would only slow it)
-    if not args.profile_run and torch.cuda.mem_get_info()[0] > n_copies * layer_bytes + (8 << 30):
+    if rotate:
         kv = [(data["k_cache"].clone(), data["v_cache"].clone(), summ.clone()) for _ in range(n_copies)]
         for kc, vc, sm in kv:
             g_rot.append(capture(lambda s, kc=kc, vc=vc, sm=sm: L.locks_decode_step(
                 H, data["q"], sm, kc, vc, data["block_table"], data["seq_lens"], w.budget_pages, bufs.selected,
                 bufs.n_selected, bufs.out, bufs.workspace, scores=bufs.scores, stream=s)))
-        config["l2"] = (f"inputs larger than L2: the timed steps rotate over {n_copies} copies of the layer's K/V "
-                        f"cache and records ({n_copies * layer_bytes / 1e9:.1f} GB), no flush; the flushed "
-                        f"single-step time is rows.step_us")
-        config["clocks_window"] = ("nvidia-smi every 100 ms over a >= 0.6 s lead-in of the same rotation "
-                                   "and the timed steps")
 
     def timed_step(i):
         """Step i of the timed (or lead-in) loop: the next copy, else a flush and the one copy."""
